@@ -1,0 +1,446 @@
+#!/usr/bin/env python3
+"""W4A16 GEMM benchmark on GB300: microseconds per call and fraction of roofline.
+
+Workload (one step = one W4A16 GEMM call): the MLP-projection shape K=5120,
+N=13824, group 128, asymmetric packed zero points, fp16 scales, M=8 tokens --
+the decode shape on which the HBM target is set. Inputs are seeded synthetic
+data (w4a16_inputs). The weights rotate over enough separate copies that the
+copies together exceed 3x the L2 size, so every call streams its weights from
+HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line. `--impl reference` times the float64 CPU oracle on the
+same workload (a bounded sample per step, extrapolated to a full call).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M, N, K, GROUP, SEED = 8, 13824, 5120, 128, 2
+WORKLOAD = f"mlp-projection W4A16 GEMM M={M} K={K} N={N} group={GROUP} asym-zp fp16-scales"
+METRIC = "W4A16 GEMM us per call (HBM roofline at M<=8)"
+
+# DRAM traffic per launch of the small-M kernel from an ncu capture, keyed by a
+# hash of the kernel source it was taken on (reported as null once the source
+# changes). Filled from profiles/ summaries.
+NCU_TRAFFIC = {}
+
+
+def algorithmic_bytes(m, n, k, group, scale_bytes=2, asym=True):
+    g = k // group
+    return (n * k // 2 + n * g * scale_bytes + (n * ((g + 1) // 2) if asym else 0)
+            + 2 * m * k + 2 * m * n)
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm_smallm.cu", "w4a16_internal.h"):
+        with open(os.path.join(ROOT, "weight_only_int4_repack_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons around a timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------
+# Reference arm and CPU baseline: the float64 oracle on the host cores.
+# ---------------------------------------------------------------------------
+def oracle_time_per_call(case, budget_s=12.0, cols_fraction=1.0):
+    import numpy as np
+    import oracle
+    ncols = max(16, int(N * cols_fraction))
+    cols = np.arange(ncols) if ncols < N else None
+    t0 = time.perf_counter()
+    reps = 0
+    Y = None
+    while True:
+        Y = oracle.gemm(case.A, case.bq, case.scales, case.zp, GROUP, cols=cols)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    return dt * (N / (ncols if cols is not None else N)) * 1e6, reps, ncols, Y
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from w4a16_inputs import make_case
+    case = make_case(M, N, K, GROUP, seed=SEED)
+    cores = oracle.default_threads()
+    # Per step: the oracle on all M rows and a column sample, sized so that the
+    # whole run stays within about two minutes.
+    t0 = time.perf_counter()
+    oracle.gemm(case.A, case.bq, case.scales, case.zp, GROUP, cols=np.arange(256))
+    per_col = (time.perf_counter() - t0) / 256
+    total = args.steps + args.warmup
+    ncols = int(max(16, min(N, 100.0 / max(total, 1) / per_col)) // 16 * 16)
+    cols = np.arange(ncols)
+    for _ in range(args.warmup):
+        oracle.gemm(case.A, case.bq, case.scales, case.zp, GROUP, cols=cols)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm(case.A, case.bq, case.scales, case.zp, GROUP, cols=cols)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    us = dt * (N / ncols) * 1e6
+    sample = f"all {M} rows x {ncols} of {N} columns per step, extrapolated to a full call"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": us, "unit": "us",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "group": GROUP},
+        "cpu_baseline": {"value": us, "unit": "us", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import weight_only_int4_repack_gb300 as w4
+    from w4a16_inputs import make_case
+
+    device = torch.device("cuda", local)
+    case = make_case(M, N, K, GROUP, seed=SEED)
+    A = torch.from_numpy(case.A).to(device)
+    q_rep = w4.w4a16_repack(torch.from_numpy(case.bq).to(device))
+    sc = torch.from_numpy(case.scales).to(device)
+    zp = torch.from_numpy(case.zp).to(device)
+    wbytes = q_rep.numel() + sc.numel() * 2 + zp.numel()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    n_rot = max(4, math.ceil(3 * l2 / wbytes))
+    rot = [(q_rep, sc, zp)] + [(q_rep.clone(), sc.clone(), zp.clone()) for _ in range(n_rot - 1)]
+    Y = torch.empty((M, N), dtype=torch.float16, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def step(i, s):
+        q, s_, z = rot[i % n_rot]
+        w4.w4a16_gemm(A, q, s_, z, GROUP, out=Y, stream=s)
+
+    path, split = w4.w4a16_gemm_plan(M, N, K, GROUP)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i, stream)
+    stream.synchronize()
+
+    # Timed region: graphs of up to R steps, replayed back to back on `stream`.
+    R = min(args.steps, 1000)
+    graphs = {}
+
+    def graph_for(n):
+        if n not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    step(i, stream)
+            graphs[n] = g
+        return graphs[n]
+
+    plan = [R] * (args.steps // R) + ([args.steps % R] if args.steps % R else [])
+    for n in set(plan):
+        graph_for(n).replay()
+    stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for n in plan:
+            graph_for(n).replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms_total = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = t.item()
+        torch.distributed.barrier()
+    us_per_call = ms_total * 1e3 / args.steps
+    value = us_per_call / world  # whole-job time per call (replicas)
+
+    # Correctness of the timed configuration (compared in the CPU-baseline leg).
+    step(0, stream)
+    stream.synchronize()
+    Y_gpu = Y.float().cpu().double().numpy()
+
+    # End to end through the public API with host buffers: H2D of A, the call,
+    # D2H of Y, every step.
+    A_h = torch.from_numpy(case.A).pin_memory()
+    Y_h = torch.empty((M, N), dtype=torch.float16).pin_memory()
+    n_e2e = min(args.steps, 2000)
+    with torch.cuda.stream(stream):
+        for i in range(10):
+            A.copy_(A_h, non_blocking=True)
+            step(i, stream)
+            Y_h.copy_(Y, non_blocking=True)
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for i in range(n_e2e):
+            A.copy_(A_h, non_blocking=True)
+            step(i, stream)
+            Y_h.copy_(Y, non_blocking=True)
+        stream.synchronize()
+        e2e_us = (time.perf_counter() - t0) * 1e6 / n_e2e
+    del graphs
+
+    hbm_peak, tf_peak, peak_src = load_peaks()
+    bytes_alg = algorithmic_bytes(M, N, K, GROUP)
+    achieved = bytes_alg / (us_per_call * 1e-6) / 1e9
+    src_hash = kernel_source_hash()
+    out = {
+        "metric": METRIC, "value": value, "unit": "us", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us_per_call / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "group": GROUP,
+                   "path": ["small_m", "tcgen05"][path], "split_k": split,
+                   "l2_policy": f"weights rotate over {n_rot} copies "
+                                f"({n_rot * wbytes / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
+                   "timing": f"CUDA graphs of {R} calls replayed back to back; CUDA events on the "
+                             "launching stream"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": NCU_TRAFFIC.get(src_hash),
+                     "peak_source": f"{peak_src} hbm_gbs", "bytes_per_call": bytes_alg,
+                     "kernel": "smallm_kernel", "kernel_source": src_hash},
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": M * K * 2,
+                "d2h_bytes_per_step": M * N * 2, "steps": n_e2e},
+        "gpu_launches": args.steps,
+    }
+
+    if rank == 0 and not args.no_extras:
+        out["extras"] = extras(args, w4, torch, device, stream, l2)
+
+    if rank == 0 and not args.no_cpu_baseline:
+        us_cpu, reps, _, Yref = oracle_time_per_call(case, budget_s=args.cpu_seconds)
+        import oracle as _o
+        err = float(np.abs(Y_gpu - Yref).max())
+        tol = 2e-2 * float(np.abs(Yref).max())
+        out["cpu_baseline"] = {"value": us_cpu, "unit": "us", "cores": _o.default_threads(),
+                               "kind": "oracle",
+                               "sample": f"full M={M} call (all {N} columns), {reps} repetitions"}
+        out["parity"] = {"max_abs_err": err, "tol": tol, "pass": err <= tol}
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def time_calls(torch, stream, fn, n_calls, reps=1):
+    """Median over `reps` of the mean device time per call (graph of n_calls calls)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            fn(i)
+    stream.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n_calls):
+            fn(i)
+    g.replay()
+    stream.synchronize()
+    out = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        stream.synchronize()
+        out.append(e0.elapsed_time(e1) * 1e3 / n_calls)
+    del g
+    return statistics.median(out)
+
+
+def extras(args, w4, torch, device, stream, l2):
+    """Secondary measurements: M sweeps, decode shape, SwiGLU fused vs unfused, repack."""
+    from w4a16_inputs import make_case, make_swiglu_case
+    hbm_peak, _, _ = load_peaks()
+    res = {}
+
+    def weights(case, copies_min=4):
+        q = w4.w4a16_repack(torch.from_numpy(case.bq).to(device))
+        s = torch.from_numpy(case.scales).to(device)
+        z = None if case.zp is None else torch.from_numpy(case.zp).to(device)
+        wb = q.numel() + s.numel() * s.element_size() + (0 if z is None else z.numel())
+        n = max(copies_min, math.ceil(3 * l2 / wb))
+        return [(q, s, z)] + [(q.clone(), s.clone(), None if z is None else z.clone())
+                              for _ in range(n - 1)]
+
+    for name, (Kx, Nx, Ms) in {"mlp": (5120, 13824, (1, 2, 4, 8, 16, 32, 64)),
+                               "decode": (4096, 4096, (1, 2, 4, 8))}.items():
+        base = make_case(max(Ms), Nx, Kx, 128, seed=2 if name == "mlp" else 1)
+        rot = weights(base)
+        rows = {}
+        for m in Ms:
+            A = torch.from_numpy(base.A[:m].copy()).to(device)
+            Yx = torch.empty((m, Nx), dtype=torch.float16, device=device)
+
+            def fn(i, A=A, Yx=Yx):
+                q, s, z = rot[i % len(rot)]
+                w4.w4a16_gemm(A, q, s, z, 128, out=Yx, stream=stream)
+            us = time_calls(torch, stream, fn, 200, reps=5)
+            b = algorithmic_bytes(m, Nx, Kx, 128)
+            path, split = w4.w4a16_gemm_plan(m, Nx, Kx, 128)
+            rows[f"M={m}"] = {"us": round(us, 3), "GB/s": round(b / us / 1e3, 1),
+                              "hbm_frac": round(b / us / 1e3 / hbm_peak, 3), "split_k": split,
+                              "path": ["small_m", "tcgen05"][path]}
+        res[name] = rows
+        del rot
+
+    # SwiGLU fused vs unfused at decode M (interleaved samples, same buffers).
+    gc, uc = make_swiglu_case(8, 13824, 5120, 128, seed=4)
+    A = torch.from_numpy(gc.A).to(device)
+    gq = w4.w4a16_repack(torch.from_numpy(gc.bq).to(device))
+    uq = w4.w4a16_repack(torch.from_numpy(uc.bq).to(device))
+    tens = [torch.from_numpy(x).to(device) for x in (gc.scales, gc.zp, uc.scales, uc.zp)]
+    n_pair = max(3, math.ceil(3 * l2 / (2 * gq.numel())))
+    sets = [(gq, uq)] + [(gq.clone(), uq.clone()) for _ in range(n_pair - 1)]
+    Yx = torch.empty((8, 13824), dtype=torch.float16, device=device)
+    ws = torch.empty(w4.w4a16_swiglu_workspace_bytes(8, 13824, 5120, 128, 0), dtype=torch.uint8,
+                     device=device)
+    samples = {True: [], False: []}
+    for _ in range(5):
+        for fused in (True, False):
+            def fn(i, fused=fused):
+                g_, u_ = sets[i % n_pair]
+                w4.w4a16_gemm_swiglu(A, g_, tens[0], tens[1], u_, tens[2], tens[3], 128,
+                                     fused=fused, out=Yx, workspace=ws, stream=stream)
+            samples[fused].append(time_calls(torch, stream, fn, 100))
+    # Fused: two weight sets, A read once, Y written once.
+    b_fused = 2 * (algorithmic_bytes(8, 13824, 5120, 128) - 2 * 8 * 5120 - 2 * 8 * 13824) \
+        + 2 * 8 * 5120 + 2 * 8 * 13824
+    res["swiglu_M8"] = {
+        "fused_us": round(statistics.median(samples[True]), 3),
+        "unfused_us": round(statistics.median(samples[False]), 3),
+        "analytic_delta_bytes": 8 * 8 * 13824,
+        "delta_note": "upper bound from shape, DRAM level: unfused writes G,U (4MN), reads them "
+                      "back (4MN); fused writes only Y",
+        "fused_GB/s": round(b_fused / statistics.median(samples[True]) / 1e3, 1),
+    }
+    del sets
+
+    # Repack (one-time): read N*K/2 + write N*K/2 bytes.
+    qsrc = torch.randint(0, 256, (13824, 2560), dtype=torch.uint8, device=device)
+    qdst = torch.empty(13824 * 2560, dtype=torch.uint8, device=device)
+    us = time_calls(torch, stream, lambda i: w4.w4a16_repack(qsrc, out=qdst, stream=stream), 20)
+    res["repack_13824x5120"] = {"us": round(us, 2),
+                                "GB/s": round(2 * qsrc.numel() / us / 1e3, 1)}
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+/*
+ * w4a16.h -- C ABI of libw4a16.so: fp16-activation x int4-weight group-quantized
+ * GEMM for NVIDIA GB300 (sm_103a).
+ *
+ * Operation (github.com/justinchuby/onnx-genai pull 960, "What's landed" and
+ * "Validation": fp16 x int4 MatMulNBits with per-group scales, group sizes
+ * 16/32/64/128 and optional asymmetric 4-bit zero points):
+ *
+ *     Y[M,N] = A[M,K] . W[N,K]^T,   W[n,k] = (q[n,k] - zp[n,k/group]) * scale[n,k/group]
+ *
+ * Input formats (the plain reading of the "ONNX-native asymmetric-zp / nibble
+ * format" named there):
+ *   A       fp16 (IEEE binary16 bit patterns), row-major [M][K]
+ *   q       uint8 [N][K/2]: nibble k of row n is byte k/2, low nibble for even k
+ *   scales  fp16 or fp32, row-major [N][G], G = K/group
+ *   zp      uint8 [N][ceil(G/2)], nibble j of row n = zero point of group j (low
+ *           nibble for even j); NULL means symmetric (zero point 8)
+ *   Y       fp16, row-major [M][N]; fp32 accumulation, round-to-nearest-even store
+ *
+ * Conventions shared by every call:
+ *   - Device pointers are caller-owned device memory; host pointers are marked.
+ *     The library never allocates, frees or synchronises inside a compute call;
+ *     work is enqueued on `stream` (a cudaStream_t passed as void*, NULL = legacy
+ *     default stream) and runs asynchronously.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     non-OK status means nothing was enqueued. Launch failures map to
+ *     W4A16_ERR_CUDA. No call throws.
+ *   - Shape rules for the repacked layout and the kernels: M, N, K > 0,
+ *     N % 16 == 0, K % 64 == 0, group in {16, 32, 64, 128}, K % group == 0.
+ *     A, q_rep and Y must be 16-byte aligned, scales aligned to their element
+ *     size. Violations return W4A16_ERR_INVALID_ARG or W4A16_ERR_UNSUPPORTED.
+ *   - Results are deterministic: the same inputs and the same split factor give
+ *     bit-identical Y on every run (fixed-order reductions, no atomics on data).
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4A16_OK = 0,
+    W4A16_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment */
+    W4A16_ERR_UNSUPPORTED = 2,   /* valid but outside the supported shape rules */
+    W4A16_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+    W4A16_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    W4A16_ERR_TIMEOUT = 5        /* a bounded device-side wait expired */
+} w4a16_status;
+
+typedef enum { W4A16_SCALE_F16 = 0, W4A16_SCALE_F32 = 1 } w4a16_scale_dtype;
+
+/* Which kernel family a GEMM call runs (reported by w4a16_gemm_plan). */
+typedef enum {
+    W4A16_PATH_SMALL_M = 0,      /* register-fed stream kernel, split-K over a cluster */
+    W4A16_PATH_TCGEN05 = 1       /* TMA + tcgen05 tensor-memory kernel */
+} w4a16_path;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *w4a16_status_string(w4a16_status s);
+
+/* Bytes of the repacked weight buffer for an N x K int4 matrix: N*K/2. */
+size_t w4a16_repacked_bytes(int N, int K);
+
+/*
+ * Repack nibble-packed int4 weights into the fragment-interleaved layout the GEMM
+ * kernels read (the MatMulNBits pull request's "bijective ... reorder for
+ * coalesced loads" with a device repack byte-identical to a host reference; the
+ * permutation itself is this library's own):
+ *   row tile n0 = 128*(n/128) with R = min(128, N-n0) rows; k-block b = k/64;
+ *   chunk (tile, b) = R*32 bytes at n0*K/2 + b*R*32; inside it 16-row sub-tile
+ *   s = (n-n0)/16 at s*512, lane l = 4*((n-n0)%8) + (k%16)/4 at l*16, u32 word
+ *   j = (k%64)/16 at j*4, nibble p = 4*(e%2) + 2*(e/2) + h with e = k%4 and
+ *   h = ((n-n0)%16)/8 (byte p/2 of the word, high nibble when p is odd).
+ *   q      device, uint8 [N][K/2] (input format above); not modified
+ *   q_rep  device, w4a16_repacked_bytes(N, K) bytes, written; must not overlap q
+ * Integer-only and bit-exact; inverse: w4a16_unpack_host.
+ */
+w4a16_status w4a16_repack(const uint8_t *q, uint8_t *q_rep, int N, int K, void *stream);
+
+/*
+ * Host inverse of w4a16_repack: q_rep (host, N*K/2 bytes) -> q (host, [N][K/2]).
+ * Synchronous, pure host code, no CUDA calls.
+ */
+w4a16_status w4a16_unpack_host(const uint8_t *q_rep, uint8_t *q, int N, int K);
+
+/*
+ * Scratch bytes a w4a16_gemm call needs (0: split-K partials are reduced through
+ * distributed shared memory inside a thread-block cluster, not global memory).
+ * split_k: 0 = automatic, 1..8 = forced factor (small-M path).
+ */
+size_t w4a16_gemm_workspace_bytes(int M, int N, int K, int group, int split_k);
+
+/*
+ * Which path and split factor w4a16_gemm would use. split_k as in w4a16_gemm.
+ * path / split_out are host pointers (either may be NULL).
+ */
+w4a16_status w4a16_gemm_plan(int M, int N, int K, int group, int split_k,
+                             int *path, int *split_out);
+
+/*
+ * Y = A . dequant(q_rep)^T  (see the operation at the top of this file).
+ *   A        device fp16 [M][K], 16-byte aligned
+ *   q_rep    device, repacked weights from w4a16_repack (N x K)
+ *   scales   device [N][K/group], dtype sdt
+ *   zp       device uint8 [N][ceil(G/2)] packed zero points, or NULL (zero point 8)
+ *   Y        device fp16 [M][N], written (no read-modify-write)
+ *   split_k  0 = automatic; 1..8 forces the small-M path's K split (a cluster
+ *            of that many CTAs per 128-row tile); ignored on the tensor-core path
+ *   ws, ws_bytes  caller scratch of at least w4a16_gemm_workspace_bytes(); may be
+ *            NULL when that is 0
+ * Small M (<= the small-M limit, 64 by default) runs the register-fed stream
+ * kernel: 128-bit coalesced weight loads, dequantisation in registers, mma.sync
+ * m16n8k16 with fp32 accumulation and the group scale applied after each group's
+ * partial sum (the pull request's "per-group scale AFTER the tensor-core
+ * accumulate"), K split across a cluster and reduced in a fixed order. Larger M
+ * runs the tcgen05 kernel: TMA-staged activations, int4 tiles dequantised to fp16
+ * ((q - zp) * scale rounded once; fp32 scales are rounded to fp16 first) into
+ * tensor memory, fp32 accumulation in tensor memory.
+ */
+w4a16_status w4a16_gemm(const uint16_t *A, const uint8_t *q_rep, const void *scales,
+                        w4a16_scale_dtype sdt, const uint8_t *zp, uint16_t *Y,
+                        int M, int N, int K, int group, int split_k,
+                        void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Scratch bytes for w4a16_gemm_swiglu: 0 when fused; 4*M*N (+alignment) when
+ * unfused (the fp16 gate and up projections are materialised).
+ */
+size_t w4a16_swiglu_workspace_bytes(int M, int N, int K, int group, int fused);
+
+/*
+ * Y = silu(A . Wg^T) * (A . Wu^T), silu(x) = x / (1 + exp(-x)) (the pull
+ * request's gate_up SwiGLU MLP fusion: paired gate/up int4 GEMMs followed by a
+ * SiluMul epilogue). Gate and up share A, K, N, group and the scale dtype.
+ *   fused = 1  one pass: both accumulators kept in fp32, silu*mul in the
+ *              epilogue, only Y is written
+ *   fused = 0  the unfused chain: gate -> fp16 G, up -> fp16 U (both in ws),
+ *              then an elementwise silu_mul(G, U) -> Y
+ * The two modes come from one source with this switch, for fusion benchmarks.
+ */
+w4a16_status w4a16_gemm_swiglu(const uint16_t *A,
+                               const uint8_t *qg_rep, const void *sg, const uint8_t *zg,
+                               const uint8_t *qu_rep, const void *su, const uint8_t *zu,
+                               w4a16_scale_dtype sdt, uint16_t *Y,
+                               int M, int N, int K, int group, int fused,
+                               void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Tuning knobs (process-wide, not thread-safe; for tests and benchmarks).
+ *   smallm_max  largest M routed to the small-M path (0 = default 64, max 64;
+ *               -1 routes every M to the tensor-core path)
+ */
+w4a16_status w4a16_set_tuning(int smallm_max);
+
+/*
+ * Read and clear the device-side error word that bounded waits set when they
+ * expire (W4A16_ERR_TIMEOUT) on the device current for the calling thread.
+ * Synchronises `stream`. Returns W4A16_OK when no kernel reported an error.
+ */
+w4a16_status w4a16_device_error(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

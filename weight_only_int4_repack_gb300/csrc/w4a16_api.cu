@@ -1,0 +1,308 @@
+// C ABI of libw4a16.so: argument validation, path and split planning, dispatch.
+// Nothing here allocates, frees or synchronises on the compute calls; every
+// check runs on the host before the first launch.
+#include <climits>
+#include <cstring>
+#include <mutex>
+
+#include "w4a16_internal.h"
+
+using namespace w4a16;
+
+namespace {
+
+int g_smallm_max = kSmallMMaxM;
+
+__device__ unsigned int g_device_error;  // set by bounded waits that expire
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+w4a16_status check_shape(int M, int N, int K, int group) {
+    if (M <= 0 || N <= 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
+    if (group != 16 && group != 32 && group != 64 && group != 128) return W4A16_ERR_UNSUPPORTED;
+    if (K % 2 != 0 || K % group != 0) return W4A16_ERR_INVALID_ARG;
+    if (N % kSubRows != 0 || K % kKBlock != 0) return W4A16_ERR_UNSUPPORTED;
+    // Index arithmetic uses 64-bit offsets; keep each dimension product sane.
+    if ((long long)M * K > (1LL << 40) || (long long)N * K > (1LL << 40) ||
+        (long long)M * N > (1LL << 40))
+        return W4A16_ERR_UNSUPPORTED;
+    return W4A16_OK;
+}
+
+w4a16_status check_weights(const uint8_t *q_rep, const void *scales, w4a16_scale_dtype sdt) {
+    if (!q_rep || !scales) return W4A16_ERR_INVALID_ARG;
+    if (sdt != W4A16_SCALE_F16 && sdt != W4A16_SCALE_F32) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(q_rep, 16)) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(scales, sdt == W4A16_SCALE_F32 ? 4 : 2)) return W4A16_ERR_INVALID_ARG;
+    return W4A16_OK;
+}
+
+struct Plan {
+    int path;
+    int split;
+    int kc;
+};
+
+w4a16_status make_plan(int M, int N, int K, int group, int split_k, bool swiglu, Plan *out) {
+    if (split_k < 0 || split_k > 8) return W4A16_ERR_INVALID_ARG;
+    Plan p{};
+    const int smax = g_smallm_max;
+    if (M <= smax) {
+        p.path = W4A16_PATH_SMALL_M;
+        const int n_tiles = (N + kTileRows - 1) / kTileRows;
+        const int nb = K / kKBlock;
+        int split = split_k;
+        if (split == 0) {
+            const int mt = (M + 7) / 8;
+            const int per_sm = (mt * (swiglu ? 2 : 1) <= 2) ? 2 : 1;
+            split = (sm_count() * per_sm) / n_tiles;
+            if (split < 1) split = 1;
+            if (split > 8) split = 8;
+            while (split > 1 && nb / split < 2) --split;
+        }
+        if (split > nb) return W4A16_ERR_UNSUPPORTED;
+        p.split = split;
+        const int per_rank = (nb + split - 1) / split;
+        const int kc_need = ((per_rank + kSmallMPrefetch - 1) / kSmallMPrefetch) * kSmallMPrefetch;
+        const int kc_max = smallm_max_kc(M, group, swiglu);
+        p.kc = kc_need < kc_max ? kc_need : kc_max;
+    } else {
+        p.path = W4A16_PATH_TCGEN05;
+        p.split = 1;
+        p.kc = 0;
+        return W4A16_ERR_UNSUPPORTED;  // tensor-core path not built in this version
+    }
+    *out = p;
+    return W4A16_OK;
+}
+
+w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------
+// Unfused SwiGLU epilogue: Y = silu(G) * U on fp16 tensors, fp32 arithmetic.
+// ---------------------------------------------------------------------------
+__global__ void silu_mul_kernel(const uint4 *__restrict__ G, const uint4 *__restrict__ U,
+                                uint4 *__restrict__ Y, size_t n_vec) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const uint4 gv = G[i], uv = U[i];
+        uint4 yv;
+        const __half2 *gh = reinterpret_cast<const __half2 *>(&gv);
+        const __half2 *uh = reinterpret_cast<const __half2 *>(&uv);
+        __half2 *yh = reinterpret_cast<__half2 *>(&yv);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 gf = __half22float2(gh[j]);
+            const float2 uf = __half22float2(uh[j]);
+            const float a = gf.x / (1.0f + expf(-gf.x)) * uf.x;
+            const float b = gf.y / (1.0f + expf(-gf.y)) * uf.y;
+            yh[j] = __floats2half2_rn(a, b);
+        }
+        Y[i] = yv;
+    }
+}
+
+}  // namespace
+
+namespace w4a16 {
+cudaError_t launch_silu_mul(const __half *G, const __half *U, __half *Y, size_t n, cudaStream_t s) {
+    const size_t n_vec = n / 8;  // n is a multiple of 8 (N % 16 == 0)
+    const int threads = 256;
+    size_t blocks = (n_vec + threads - 1) / threads;
+    const size_t cap = (size_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks == 0) blocks = 1;
+    silu_mul_kernel<<<(unsigned)blocks, threads, 0, s>>>(reinterpret_cast<const uint4 *>(G),
+                                                        reinterpret_cast<const uint4 *>(U),
+                                                        reinterpret_cast<uint4 *>(Y), n_vec);
+    return cudaGetLastError();
+}
+}  // namespace w4a16
+
+extern "C" {
+
+const char *w4a16_status_string(w4a16_status s) {
+    switch (s) {
+        case W4A16_OK: return "ok";
+        case W4A16_ERR_INVALID_ARG: return "invalid argument";
+        case W4A16_ERR_UNSUPPORTED: return "unsupported shape or configuration";
+        case W4A16_ERR_WORKSPACE: return "workspace missing or too small";
+        case W4A16_ERR_CUDA: return "CUDA error";
+        case W4A16_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+size_t w4a16_repacked_bytes(int N, int K) {
+    if (N <= 0 || K <= 0) return 0;
+    return (size_t)N * (size_t)K / 2;
+}
+
+w4a16_status w4a16_repack(const uint8_t *q, uint8_t *q_rep, int N, int K, void *stream) {
+    if (!q || !q_rep || N <= 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
+    if (N % kSubRows || K % kKBlock) return W4A16_ERR_UNSUPPORTED;
+    if (!aligned(q, 2) || !aligned(q_rep, 16)) return W4A16_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)N * K / 2;
+    const uintptr_t a = (uintptr_t)q, b = (uintptr_t)q_rep;
+    if (a < b + bytes && b < a + bytes) return W4A16_ERR_INVALID_ARG;  // must not overlap
+    return from_cuda(launch_repack(q, q_rep, N, K, (cudaStream_t)stream));
+}
+
+w4a16_status w4a16_unpack_host(const uint8_t *q_rep, uint8_t *q, int N, int K) {
+    if (!q_rep || !q || N <= 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
+    if (N % kSubRows || K % kKBlock) return W4A16_ERR_UNSUPPORTED;
+    const size_t row_bytes = (size_t)K / 2;
+    for (int n0 = 0; n0 < N; n0 += kTileRows) {
+        const int R = (N - n0) < kTileRows ? (N - n0) : kTileRows;
+        for (int b = 0; b < K / kKBlock; ++b) {
+            const uint8_t *chunk = q_rep + chunk_offset(n0, N, K, b);
+            for (int s = 0; s < R / kSubRows; ++s)
+                for (int lane = 0; lane < 32; ++lane) {
+                    const int g = lane / 4, t = lane % 4;
+                    for (int j = 0; j < 4; ++j) {
+                        const uint8_t *wp = chunk + s * kSubBytes + lane * 16 + j * 4;
+                        const uint32_t word = (uint32_t)wp[0] | ((uint32_t)wp[1] << 8) |
+                                              ((uint32_t)wp[2] << 16) | ((uint32_t)wp[3] << 24);
+                        for (int h = 0; h < 2; ++h) {
+                            const int row = n0 + s * kSubRows + g + 8 * h;
+                            for (int e = 0; e < 4; ++e) {
+                                const int p = 4 * (e % 2) + 2 * (e / 2) + h;
+                                const uint8_t nib = (uint8_t)((word >> (4 * p)) & 0xF);
+                                const int k = b * kKBlock + 16 * j + 4 * t + e;
+                                uint8_t &dst = q[(size_t)row * row_bytes + k / 2];
+                                dst = (k % 2 == 0) ? (uint8_t)((dst & 0xF0) | nib)
+                                                   : (uint8_t)((dst & 0x0F) | (nib << 4));
+                            }
+                        }
+                    }
+                }
+        }
+    }
+    return W4A16_OK;
+}
+
+size_t w4a16_gemm_workspace_bytes(int M, int N, int K, int group, int split_k) {
+    (void)M; (void)N; (void)K; (void)group; (void)split_k;
+    return 0;
+}
+
+w4a16_status w4a16_gemm_plan(int M, int N, int K, int group, int split_k, int *path, int *split_out) {
+    w4a16_status st = check_shape(M, N, K, group);
+    if (st != W4A16_OK) return st;
+    Plan p;
+    st = make_plan(M, N, K, group, split_k, false, &p);
+    if (st != W4A16_OK) return st;
+    if (path) *path = p.path;
+    if (split_out) *split_out = p.split;
+    return W4A16_OK;
+}
+
+static w4a16_status gemm_impl(const uint16_t *A, const WeightSet *ws_sets, int nsets,
+                              w4a16_scale_dtype sdt, uint16_t *Y, int M, int N, int K, int group,
+                              int split_k, cudaStream_t stream) {
+    Plan plan;
+    w4a16_status st = make_plan(M, N, K, group, split_k, nsets == 2, &plan);
+    if (st != W4A16_OK) return st;
+    SmallMParams p{};
+    p.A = reinterpret_cast<const __half *>(A);
+    p.w[0] = ws_sets[0];
+    p.w[1] = nsets == 2 ? ws_sets[1] : ws_sets[0];
+    p.Y = reinterpret_cast<__half *>(Y);
+    p.M = M; p.N = N; p.K = K; p.G = K / group;
+    p.scale_f32 = sdt == W4A16_SCALE_F32;
+    p.split = plan.split;
+    p.kc_blocks = plan.kc;
+    return from_cuda(launch_smallm(p, group, nsets == 2, stream));
+}
+
+w4a16_status w4a16_gemm(const uint16_t *A, const uint8_t *q_rep, const void *scales,
+                        w4a16_scale_dtype sdt, const uint8_t *zp, uint16_t *Y,
+                        int M, int N, int K, int group, int split_k,
+                        void *ws, size_t ws_bytes, void *stream) {
+    (void)ws; (void)ws_bytes;
+    w4a16_status st = check_shape(M, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (!A || !Y) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(Y, 16)) return W4A16_ERR_INVALID_ARG;
+    st = check_weights(q_rep, scales, sdt);
+    if (st != W4A16_OK) return st;
+    const WeightSet w{q_rep, scales, zp};
+    return gemm_impl(A, &w, 1, sdt, Y, M, N, K, group, split_k, (cudaStream_t)stream);
+}
+
+size_t w4a16_swiglu_workspace_bytes(int M, int N, int K, int group, int fused) {
+    (void)K; (void)group;
+    if (fused || M <= 0 || N <= 0) return 0;
+    return 2 * align_up((size_t)M * N * 2, 256);
+}
+
+w4a16_status w4a16_gemm_swiglu(const uint16_t *A,
+                               const uint8_t *qg_rep, const void *sg, const uint8_t *zg,
+                               const uint8_t *qu_rep, const void *su, const uint8_t *zu,
+                               w4a16_scale_dtype sdt, uint16_t *Y,
+                               int M, int N, int K, int group, int fused,
+                               void *ws, size_t ws_bytes, void *stream) {
+    w4a16_status st = check_shape(M, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (!A || !Y) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(Y, 16)) return W4A16_ERR_INVALID_ARG;
+    if ((st = check_weights(qg_rep, sg, sdt)) != W4A16_OK) return st;
+    if ((st = check_weights(qu_rep, su, sdt)) != W4A16_OK) return st;
+    const WeightSet sets[2] = {{qg_rep, sg, zg}, {qu_rep, su, zu}};
+    cudaStream_t s = (cudaStream_t)stream;
+    if (fused) return gemm_impl(A, sets, 2, sdt, Y, M, N, K, group, 0, s);
+
+    const size_t need = w4a16_swiglu_workspace_bytes(M, N, K, group, 0);
+    if (!ws || ws_bytes < need || !aligned(ws, 256)) return W4A16_ERR_WORKSPACE;
+    Plan plan;
+    if ((st = make_plan(M, N, K, group, 0, false, &plan)) != W4A16_OK) return st;
+    uint16_t *Gb = reinterpret_cast<uint16_t *>(ws);
+    uint16_t *Ub = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(ws) +
+                                                 align_up((size_t)M * N * 2, 256));
+    if ((st = gemm_impl(A, &sets[0], 1, sdt, Gb, M, N, K, group, 0, s)) != W4A16_OK) return st;
+    if ((st = gemm_impl(A, &sets[1], 1, sdt, Ub, M, N, K, group, 0, s)) != W4A16_OK) return st;
+    return from_cuda(launch_silu_mul(reinterpret_cast<const __half *>(Gb),
+                                     reinterpret_cast<const __half *>(Ub),
+                                     reinterpret_cast<__half *>(Y), (size_t)M * N, s));
+}
+
+w4a16_status w4a16_set_tuning(int smallm_max) {
+    if (smallm_max < -1 || smallm_max > kSmallMMaxM) return W4A16_ERR_INVALID_ARG;
+    g_smallm_max = smallm_max == 0 ? kSmallMMaxM : (smallm_max < 0 ? 0 : smallm_max);
+    return W4A16_OK;
+}
+
+w4a16_status w4a16_device_error(void *stream) {
+    unsigned int v = 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyFromSymbolAsync(&v, g_device_error, sizeof(v), 0, cudaMemcpyDeviceToHost, s) !=
+        cudaSuccess)
+        return W4A16_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
+    if (v != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice,
+                                    s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return W4A16_ERR_CUDA;
+        return (w4a16_status)v;
+    }
+    return W4A16_OK;
+}
+
+}  // extern "C"

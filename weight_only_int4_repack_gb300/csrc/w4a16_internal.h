@@ -1,0 +1,65 @@
+// Internal declarations shared by the CUDA translation units of libw4a16.so.
+// Not installed; the public interface is include/w4a16.h.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/w4a16.h"
+
+namespace w4a16 {
+
+// Repacked layout geometry (see w4a16_repack in include/w4a16.h).
+constexpr int kTileRows = 128;   // rows per row tile
+constexpr int kSubRows = 16;     // rows per sub-tile (one warp's MMA row block)
+constexpr int kKBlock = 64;      // k per k-block
+constexpr int kSubBytes = 512;   // bytes of one 16-row x 64-k sub-tile
+
+// Byte offset of chunk (row tile starting at n0, k-block b).
+__host__ __device__ inline size_t chunk_offset(int n0, int N, int K, int b) {
+    int R = (N - n0) < kTileRows ? (N - n0) : kTileRows;
+    return (size_t)n0 * (size_t)(K / 2) + (size_t)b * (size_t)R * 32u;
+}
+
+// ---------------------------------------------------------------------------
+// Launch parameters
+// ---------------------------------------------------------------------------
+struct WeightSet {
+    const uint8_t *q_rep;   // repacked int4 weights
+    const void *scales;     // [N][G] fp16 or fp32
+    const uint8_t *zp;      // [N][ceil(G/2)] or nullptr
+};
+
+struct SmallMParams {
+    const __half *A;        // [M][K]
+    WeightSet w[2];         // gate/up (w[1] only for SwiGLU)
+    __half *Y;              // [M][N]
+    int M, N, K, G;
+    int scale_f32;
+    int split;              // CTAs per row tile along K (cluster size)
+    int kc_blocks;          // k-blocks per staged chunk (multiple of kPrefetch)
+};
+
+struct TcParams {
+    const __half *A;
+    WeightSet w[2];
+    __half *Y;
+    int M, N, K, G;
+    int scale_f32;
+    unsigned int *err;      // device error word for bounded waits
+};
+
+// Host-side launchers (return cudaError_t of the launch).
+cudaError_t launch_repack(const uint8_t *q, uint8_t *q_rep, int N, int K, cudaStream_t s);
+cudaError_t launch_smallm(const SmallMParams &p, int group, bool swiglu, cudaStream_t s);
+size_t smallm_smem_bytes(int M, int group, bool swiglu, int kc_blocks);
+int smallm_max_kc(int M, int group, bool swiglu);
+cudaError_t launch_silu_mul(const __half *G, const __half *U, __half *Y, size_t n,
+                            cudaStream_t s);
+
+constexpr int kSmallMPrefetch = 8;   // weight k-blocks in flight per warp
+constexpr int kSmallMThreads = 256;  // 8 warps = 8 sub-tiles of one row tile
+constexpr int kSmallMMaxM = 64;      // 8 token tiles of 8
+
+}  // namespace w4a16
