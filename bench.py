@@ -232,20 +232,26 @@ def run_ours(args):
         return graphs[n]
 
     plan = [R] * (args.steps // R) + ([args.steps % R] if args.steps % R else [])
-    for n in set(plan):
-        graph_for(n).replay()
+    # CUDAGraph.replay() launches on the current stream: keep `stream` current.
+    with torch.cuda.stream(stream):
+        for n in set(plan):
+            graph_for(n).replay()
     stream.synchronize()
     if world > 1:
         torch.distributed.barrier()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    Y.zero_()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk, torch.cuda.stream(stream):
         torch.cuda.synchronize()
         ev0.record(stream)
         for n in plan:
             graph_for(n).replay()
         ev1.record(stream)
         torch.cuda.synchronize()
+    if not bool((Y != 0).any()):
+        raise RuntimeError("timed graphs did not write the output")
     ms_total = ev0.elapsed_time(ev1)
     if world > 1:
         t = torch.tensor([ms_total], device=device)
@@ -332,17 +338,18 @@ def time_calls(torch, stream, fn, n_calls, reps=1):
     with torch.cuda.graph(g, stream=stream):
         for i in range(n_calls):
             fn(i)
-    g.replay()
-    stream.synchronize()
     out = []
-    for _ in range(reps):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
         g.replay()
-        e1.record(stream)
         stream.synchronize()
-        out.append(e0.elapsed_time(e1) * 1e3 / n_calls)
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            stream.synchronize()
+            out.append(e0.elapsed_time(e1) * 1e3 / n_calls)
     del g
     return statistics.median(out)
 

@@ -72,9 +72,12 @@ size_t w4a16_repacked_bytes(int N, int K);
  * permutation itself is this library's own):
  *   row tile n0 = 128*(n/128) with R = min(128, N-n0) rows; k-block b = k/64;
  *   chunk (tile, b) = R*32 bytes at n0*K/2 + b*R*32; inside it 16-row sub-tile
- *   s = (n-n0)/16 at s*512, lane l = 4*((n-n0)%8) + (k%16)/4 at l*16, u32 word
- *   j = (k%64)/16 at j*4, nibble p = 4*(e%2) + 2*(e/2) + h with e = k%4 and
- *   h = ((n-n0)%16)/8 (byte p/2 of the word, high nibble when p is odd).
+ *   s = (n-n0)/16 at s*512; with g = (n-n0)%8 and t = (k%16)/4 the 16-byte lane
+ *   slot 4*g + (t + g/2)%4 at slot*16; u32 word j = (k%64)/16 at j*4; nibble
+ *   p = 4*(e%2) + 2*(e/2) + h with e = k%4 and h = ((n-n0)%16)/8 (byte p/2 of the
+ *   word, high nibble when p is odd). Each lane slot is one mma.sync m16n8k16
+ *   A fragment per word (rows g and g+8); a 16-row x 64-k sub-tile is 512
+ *   contiguous bytes and a (tile, k-block) chunk one contiguous bulk copy.
  *   q      device, uint8 [N][K/2] (input format above); not modified
  *   q_rep  device, w4a16_repacked_bytes(N, K) bytes, written; must not overlap q
  * Integer-only and bit-exact; inverse: w4a16_unpack_host.

@@ -17,7 +17,7 @@ repacked buffer, which has the same N*K/2 bytes:
     k-block    b  = k // 64
     chunk      starts at byte n0*K/2 + b*R*32, spans R*32 bytes
     sub-tile   s  = (n - n0) // 16                         -> s*512 within the chunk
-    lane       l  = 4*g + t,  g = (n - n0) % 8,  t = (k % 16) // 4   -> l*16
+    lane slot  l  = 4*g + (t + g//2) % 4,  g = (n - n0) % 8,  t = (k % 16) // 4   -> l*16
     word       j  = (k % 64) // 16                         -> j*4 (little-endian u32)
     nibble     p  = 4*(e % 2) + 2*(e // 2) + h,  e = k % 4,  h = ((n - n0) % 16) // 8
                byte j*4 + p//2 of the lane, high nibble when p is odd
@@ -26,8 +26,12 @@ N must be a multiple of 16 and K a multiple of 64.
 
 Reading of the layout (what the two GPU consumers rely on; the tests check both
 against the PTX ISA's fragment tables):
-  * a 16-row x 64-k sub-tile is 512 contiguous bytes; lane l's 16 bytes hold rows
-    g and g+8 at k = 16j + 4t + {0,1,2,3} for j = 0..3;
+  * a 16-row x 64-k sub-tile is 512 contiguous bytes; the 16 bytes of the MMA
+    fragment owner (g, t) sit in lane slot 4g + (t + g//2) % 4 and hold rows g and
+    g+8 at k = 16j + 4t + {0,1,2,3} for j = 0..3. The rotation by g//2 keeps the
+    four slots of a row group inside one 64-byte span while spreading the reads of
+    a one-row-per-thread consumer (slot 4g + (t + g//2) % 4 for fixed t, g = 0..7)
+    over all eight 16-byte bank groups of shared memory;
   * in word j, nibbles (i, i+4) for i = 0,1,2,3 are the element pairs
     (row g, e 0/1), (row g+8, e 0/1), (row g, e 2/3), (row g+8, e 2/3).
 """
@@ -56,7 +60,7 @@ def nibble_position(n, k, N: int, K: int):
     t = (k % 16) // 4
     j = (k % 64) // 16
     e = k % 4
-    lane = 4 * g + t
+    lane = 4 * g + (t + g // 2) % 4
     p = 4 * (e % 2) + 2 * (e // 2) + h
     byte = chunk + s * 512 + lane * 16 + j * 4 + p // 2
     return byte, (p % 2).astype(bool)

@@ -57,6 +57,16 @@ def test_one_hot_nibble_moves_to_one_place():
         assert rep[nz[0]] in (0x0A, 0xA0)
 
 
+def test_one_row_per_thread_reads_spread_over_bank_groups():
+    # For fixed t, the eight row groups g of a sub-tile read eight different
+    # 16-byte bank groups (offset mod 128 bytes) of a shared-memory copy.
+    for t in range(4):
+        groups = {(_slot(g, t) * 16) % 128 for g in range(8)}
+        assert len(groups) == 8
+    for g in range(8):   # the four slots of one row group stay in one 64-byte span
+        assert sorted(_slot(g, t) for t in range(4)) == list(range(4 * g, 4 * g + 4))
+
+
 def test_rejects_unsupported_dims():
     for N, K in [(8, 64), (16, 32), (20, 64)]:
         with pytest.raises(ValueError):
@@ -68,6 +78,11 @@ def _words(rep, N, K, n0, b, s):
     R = min(128, N - n0)
     base = n0 * (K // 2) + b * R * 32 + s * 512
     return rep[base:base + 512].view("<u4").reshape(32, 4)
+
+
+def _slot(g, t):
+    """Lane slot (16-byte unit of a sub-tile) of the fragment owned by (g, t)."""
+    return 4 * g + (t + g // 2) % 4
 
 
 def _half(word, nib):
@@ -92,7 +107,7 @@ def test_mma_m16n8k16_fragments_compute_true_dot(N, K):
                     Bvirt = np.zeros((16, 8), dtype=np.int64)
                     for lane in range(32):
                         gid, tig = lane >> 2, lane & 3
-                        word = w[lane, j]
+                        word = w[_slot(gid, tig), j]
                         a = [_half(word, i) for i in (0, 4, 1, 5, 2, 6, 3, 7)]  # a0..a7
                         Avirt[gid, 2 * tig], Avirt[gid, 2 * tig + 1] = a[0], a[1]
                         Avirt[gid + 8, 2 * tig], Avirt[gid + 8, 2 * tig + 1] = a[2], a[3]
@@ -121,7 +136,7 @@ def test_tmem_row_per_lane_extraction(N, K):
                 cols = np.zeros((32, 2), dtype=np.uint8)      # 32 columns x (lo, hi)
                 for t in range(4):
                     for j in range(4):
-                        word = w[4 * g + t, j]
+                        word = w[_slot(g, t), j]
                         cols[8 * j + 2 * t] = (_half(word, h), _half(word, h + 4))
                         cols[8 * j + 2 * t + 1] = (_half(word, h + 2), _half(word, h + 6))
                 row_k = cols.reshape(-1)                      # k = 2c + {0, 1}

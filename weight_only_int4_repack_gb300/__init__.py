@@ -20,6 +20,10 @@ if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
                       f"g.build()'` (needs nvcc); there is no fallback implementation")
 
+# torch first: the library links the shared CUDA runtime by soname, so it must
+# resolve to the runtime torch already loaded (one runtime per process).
+import torch  # noqa: E402,F401
+
 lib = ctypes.CDLL(LIB_PATH)
 
 # Status codes and enums (mirror include/w4a16.h).

@@ -5,7 +5,7 @@
 // bijective interleaved order so that warps load contiguous bytes; its device
 // repack is byte-identical to a host reference. This is the same idea for this
 // library's own layout (stated in include/w4a16.h). Integer work, HBM-bound:
-// every thread produces one 16-byte lane chunk (two rows x 16 k of four k16
+// every thread produces one 16-byte lane slot (two rows x 16 k of four k16
 // steps) and writes it with one coalesced 128-bit store.
 #include "w4a16_internal.h"
 
@@ -24,8 +24,9 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
     const int b = (int)(off / (2 * R));
     const int rem = (int)(off % (2 * R));
     const int s = rem >> 5;
-    const int lane = rem & 31;
-    const int g = lane >> 2, t = lane & 3;
+    const int slot = rem & 31;
+    // Slot 4g + (t + g/2) % 4 holds the fragment owned by (g, t).
+    const int g = slot >> 2, t = ((slot & 3) - (g >> 1)) & 3;
     const size_t row_bytes = (size_t)(K / 2);
     const uint8_t *r0 = q + (size_t)(n0 + s * kSubRows + g) * row_bytes;
     const uint8_t *r1 = r0 + 8 * row_bytes;

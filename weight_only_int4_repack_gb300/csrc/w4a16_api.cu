@@ -17,6 +17,19 @@ __device__ unsigned int g_device_error;  // set by bounded waits that expire
 
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
+// Device address of the error word on the current device (looked up once per device).
+unsigned int *device_error_ptr() {
+    static unsigned int *cached[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!cached[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return nullptr;
+        cached[dev] = static_cast<unsigned int *>(ptr);
+    }
+    return cached[dev];
+}
+
 int sm_count() {
     static int cached[64] = {0};
     int dev = 0;
@@ -66,8 +79,8 @@ w4a16_status make_plan(int M, int N, int K, int group, int split_k, bool swiglu,
         const int nb = K / kKBlock;
         int split = split_k;
         if (split == 0) {
-            const int mt = (M + 7) / 8;
-            const int per_sm = (mt * (swiglu ? 2 : 1) <= 2) ? 2 : 1;
+            // As many K ranks per tile as keep the whole grid resident in one wave.
+            const int per_sm = smallm_ctas_per_sm(M, swiglu);
             split = (sm_count() * per_sm) / n_tiles;
             if (split < 1) split = 1;
             if (split > 8) split = 8;
@@ -76,9 +89,8 @@ w4a16_status make_plan(int M, int N, int K, int group, int split_k, bool swiglu,
         if (split > nb) return W4A16_ERR_UNSUPPORTED;
         p.split = split;
         const int per_rank = (nb + split - 1) / split;
-        const int kc_need = ((per_rank + kSmallMPrefetch - 1) / kSmallMPrefetch) * kSmallMPrefetch;
         const int kc_max = smallm_max_kc(M, group, swiglu);
-        p.kc = kc_need < kc_max ? kc_need : kc_max;
+        p.kc = per_rank < kc_max ? per_rank : kc_max;
     } else {
         p.path = W4A16_PATH_TCGEN05;
         p.split = 1;
@@ -172,10 +184,10 @@ w4a16_status w4a16_unpack_host(const uint8_t *q_rep, uint8_t *q, int N, int K) {
         for (int b = 0; b < K / kKBlock; ++b) {
             const uint8_t *chunk = q_rep + chunk_offset(n0, N, K, b);
             for (int s = 0; s < R / kSubRows; ++s)
-                for (int lane = 0; lane < 32; ++lane) {
-                    const int g = lane / 4, t = lane % 4;
+                for (int slot = 0; slot < 32; ++slot) {
+                    const int g = slot / 4, t = ((slot % 4) - g / 2 + 4) % 4;
                     for (int j = 0; j < 4; ++j) {
-                        const uint8_t *wp = chunk + s * kSubBytes + lane * 16 + j * 4;
+                        const uint8_t *wp = chunk + s * kSubBytes + slot * 16 + j * 4;
                         const uint32_t word = (uint32_t)wp[0] | ((uint32_t)wp[1] << 8) |
                                               ((uint32_t)wp[2] << 16) | ((uint32_t)wp[3] << 24);
                         for (int h = 0; h < 2; ++h) {
@@ -227,6 +239,8 @@ static w4a16_status gemm_impl(const uint16_t *A, const WeightSet *ws_sets, int n
     p.scale_f32 = sdt == W4A16_SCALE_F32;
     p.split = plan.split;
     p.kc_blocks = plan.kc;
+    p.err = device_error_ptr();
+    if (!p.err) return W4A16_ERR_CUDA;
     return from_cuda(launch_smallm(p, group, nsets == 2, stream));
 }
 

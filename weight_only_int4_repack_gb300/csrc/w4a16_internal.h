@@ -38,7 +38,8 @@ struct SmallMParams {
     int M, N, K, G;
     int scale_f32;
     int split;              // CTAs per row tile along K (cluster size)
-    int kc_blocks;          // k-blocks per staged chunk (multiple of kPrefetch)
+    int kc_blocks;          // k-blocks per staged activation chunk
+    unsigned int *err;      // device error word for bounded waits
 };
 
 struct TcParams {
@@ -55,11 +56,11 @@ cudaError_t launch_repack(const uint8_t *q, uint8_t *q_rep, int N, int K, cudaSt
 cudaError_t launch_smallm(const SmallMParams &p, int group, bool swiglu, cudaStream_t s);
 size_t smallm_smem_bytes(int M, int group, bool swiglu, int kc_blocks);
 int smallm_max_kc(int M, int group, bool swiglu);
+int smallm_ctas_per_sm(int M, bool swiglu);
 cudaError_t launch_silu_mul(const __half *G, const __half *U, __half *Y, size_t n,
                             cudaStream_t s);
 
-constexpr int kSmallMPrefetch = 8;   // weight k-blocks in flight per warp
-constexpr int kSmallMThreads = 256;  // 8 warps = 8 sub-tiles of one row tile
+constexpr int kSmallMThreads = 288;  // 8 consumer warps (one sub-tile each) + 1 producer warp
 constexpr int kSmallMMaxM = 64;      // 8 token tiles of 8
 
 }  // namespace w4a16
