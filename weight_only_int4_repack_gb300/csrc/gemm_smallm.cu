@@ -6,38 +6,75 @@
 // occupancy-bound and split the K range over more CTAs, reducing fp32 partials
 // in a fixed order. This kernel keeps those two ideas and re-designs the rest
 // for sm_103a:
-//   * one CTA = one 128-row tile (8 consumer warps, one 16-row sub-tile each) x
-//     one K range, plus a producer warp. The producer streams each (tile, 64-k
-//     block) chunk -- 4 KB contiguous in the repacked layout -- into a 48 KB
-//     shared-memory ring with cp.async.bulk (the TMA engine), so tens of KB per
-//     CTA are in flight without costing registers;
-//   * each consumer lane reads one 16-byte slot (a 128-bit, conflict-free shared
-//     load); its four words are already mma.sync.m16n8k16 A fragments: one
-//     and/or per half2 turns two nibbles into fp16 (1024 + q), one sub.f16x2
-//     removes (1024 + zp) exactly, and the tokens are the n=8 operand;
-//   * fp32 accumulation; the group scale is applied to each group's fp32 partial
-//     sum (the pull request's "per-group scale AFTER the tensor-core accumulate");
+//   * one CTA = one 128-row tile x one K range. In the repacked layout that
+//     range is one contiguous span, so a producer warp streams it through a
+//     shared-memory ring with 16 KB cp.async.bulk copies (four 64-k blocks per
+//     stage), starting at kernel entry: the weight stream is already in flight
+//     while the CTA stages activations and metadata. (Measured on GB300: 1-D
+//     bulk copies reach HBM speed with 8-16 KB pieces; with 4 KB pieces a CTA
+//     completed only about one copy per half microsecond.)
+//   * consumer warps own one or two 16-row sub-tiles; a lane reads one 16-byte
+//     slot per sub-tile and block (a conflict-free 128-bit shared load) whose
+//     four words are mma.sync.m16n8k16 A fragments for four k16 steps; the
+//     tokens are the n=8 operand and accumulation is fp32;
+//   * dequantisation is 5 integer ops per 8 weights: OR-ing a nibble into the
+//     mantissa of fp16 1024 gives exactly 1024 + q (bits 0-3) or 1024 + 16 q
+//     (bits 4-7); in this layout the x16 form always belongs to the fragment's
+//     second row (g+8). Per group and row the MMA gives acc_g = sum (1024 + f q) a
+//     with f in {1, 16}, and
+//         sum_g s_g sum (q - zp_g) a = sum_g (s_g/f) acc_g - sum_g (s_g/f)(1024 + f zp_g) A_g
+//     where A_g is the group's activation sum. The first term is one fp32 FMA
+//     per output and group (the pull request's "per-group scale AFTER the
+//     tensor-core accumulate"); the second depends only on metadata and
+//     activations and is subtracted once per staged chunk;
 //   * the K split is a thread-block cluster: partial tiles are summed through
 //     distributed shared memory in rank order (deterministic, no global scratch,
 //     one launch).
 // CUDA-core FMA would need M FMAs per weight; at M = 8 that is about 0.57 G FMA
 // for K=5120, N=13824, more than the FP32 pipes finish in the HBM time of the
 // weight stream, so the contraction runs on the tensor cores.
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <type_traits>
+
 #include "ptx.cuh"
 #include "w4a16_internal.h"
 
 namespace w4a16 {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kRingBytes = 48 * 1024;
-constexpr int kChunkMax = kTileRows * 32;  // bytes of one (tile, k-block) chunk
-constexpr int kPartStride = kTileRows + 4;  // floats per partial row (bank spread)
+constexpr int kPartStride = kTileRows + 4;          // floats per partial row (bank spread)
+constexpr int kBPS = 4;                             // k-blocks per ring stage
+constexpr int kStageSet = kTileRows * 32 * kBPS;    // 16 KB: one stage of one weight set
 
-__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+// Sub-tiles per consumer warp: two when the accumulators are small (shares the
+// activation fragments and the per-block overhead), else one.
+template <int MT, bool SWIGLU>
+struct Shape {
+    static constexpr int NS = SWIGLU ? 2 : 1;
+    static constexpr int SUBT = (MT * NS <= 2) ? 2 : 1;
+    static constexpr int CW = 8 / SUBT;             // consumer warps
+    static constexpr int THREADS = CW * 32 + 32;    // + one producer warp
+    static constexpr int STAGES = 2;                // 32 / 64 KB of weights in flight per CTA
+    static constexpr int MINB = SUBT == 2 ? 4 : (MT * NS <= 4 ? 2 : 1);
+};
+
+// Compile-time loop: f(std::integral_constant<int, I>) for I in [B, E). Register
+// arrays indexed by the constant stay in registers.
+template <int B, int E, typename F>
+__device__ __forceinline__ void static_for(F &&f) {
+    if constexpr (B < E) {
+        f(std::integral_constant<int, B>{});
+        static_for<B + 1, E>(f);
+    }
+}
+
+// (x & MASK) | 0x64006400 in one lop3: nibbles OR-ed into the mantissa of fp16 1024.
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t lop_or(uint32_t x) {
     uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "n"(MASK), "n"(0x64006400));
     return r;
 }
 
@@ -53,39 +90,39 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 
 __device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
 
-// Shared-memory plan of one CTA (byte offsets from the dynamic base).
+// Shared-memory plan of one CTA (byte offsets from the dynamic base). The
+// activation rows are the M token rows plus one zero row that padding tokens of
+// the last 8-token tile read from.
 struct SmemPlan {
-    int stages, a_stride, ng;
-    size_t a_off, meta_off, meta_set_bytes, bar_off, total;
+    int a_stride, ng;
+    size_t a_off, meta_off, meta_set_bytes, gsum_off, bar_off, total;
 };
 
-__host__ __device__ inline SmemPlan make_plan(int MT, int group, int kc, int ns) {
+__host__ __device__ inline SmemPlan make_plan(int M, int MT, int group, int kc, int ns, int stages) {
     SmemPlan p;
-    p.stages = kRingBytes / (ns * kChunkMax);
-    p.a_off = (size_t)p.stages * ns * kChunkMax;
-    p.a_stride = kc * kKBlock + 16;  // +32 bytes per row: conflict-free 8-byte fragment loads
-    p.ng = (kc * kKBlock) / group + 1;
-    p.meta_off = p.a_off + (size_t)8 * MT * p.a_stride * 2;
-    p.meta_set_bytes = (size_t)kTileRows * p.ng * 8;  // float scale + half2 (1024 + zp)
-    const size_t main_end = p.meta_off + ns * p.meta_set_bytes;
-    const size_t part_end = (size_t)ns * 8 * MT * kPartStride * 4;  // aliases the ring after use
+    p.a_off = (size_t)stages * ns * kStageSet;     // the weight ring comes first
+    p.a_stride = kc * kKBlock + 16;                 // +32 bytes per row: conflict-free fragment loads
+    p.ng = (kc * kKBlock + group - 1) / group;      // groups of a chunk (chunks start on a group)
+    p.meta_off = p.a_off + (size_t)(M + 1) * p.a_stride * 2;
+    p.meta_set_bytes = (size_t)kTileRows * p.ng * 8;  // float2 (s / f, (s / f)(1024 + f zp))
+    p.gsum_off = p.meta_off + ns * p.meta_set_bytes;  // float [ng][8 MT] group activation sums
+    const size_t main_end = p.gsum_off + (size_t)p.ng * 8 * MT * 4;
+    const size_t part_end = (size_t)ns * 8 * MT * kPartStride * 4;  // overlays the ring after use
     const size_t end = main_end > part_end ? main_end : part_end;
     p.bar_off = (end + 15) / 16 * 16;
-    p.total = p.bar_off + (size_t)(2 * p.stages + 2) * 8;
+    p.total = p.bar_off + (size_t)(2 * stages + 2) * 8;  // full[], empty[], activation barrier, abort
     return p;
 }
 
-template <int MT, bool SWIGLU>
-struct MinBlocks {
-    static constexpr int value = (MT * (SWIGLU ? 2 : 1) <= 4) ? 2 : 1;
-};
-
 template <int GROUP, int MT, bool SWIGLU>
-__global__ void __launch_bounds__(kSmallMThreads, (MinBlocks<MT, SWIGLU>::value))
+__global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>::MINB)
     smallm_kernel(const SmallMParams p) {
-    constexpr int NS = SWIGLU ? 2 : 1;
-    constexpr int FL = GROUP < kKBlock ? GROUP : kKBlock;  // k per scale flush
-    constexpr int SPF = FL / 16;                             // k16 steps per flush
+    using Sh = Shape<MT, SWIGLU>;
+    constexpr int NS = Sh::NS, SUBT = Sh::SUBT, CW = Sh::CW, STAGES = Sh::STAGES;
+    constexpr int NC = CW * 32;                            // consumer threads
+    constexpr int SPG = GROUP / 16;                        // k16 steps per group
+    constexpr int BPG = GROUP > kKBlock ? GROUP / kKBlock : 1;  // k-blocks per group (128: 2)
+    static_assert((kBPS * 4) % SPG == 0, "a ring stage must hold whole groups");
 
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x;
@@ -96,54 +133,105 @@ __global__ void __launch_bounds__(kSmallMThreads, (MinBlocks<MT, SWIGLU>::value)
     const int nsub = R / kSubRows;
     const int S = p.split;
     const int rank = (S > 1) ? (int)ptx::cluster_rank() : 0;
-    const int nb = p.K / kKBlock;
-    const int b_begin = (int)((long long)nb * rank / S);
-    const int b_end = (int)((long long)nb * (rank + 1) / S);
-    const int nblk = b_end - b_begin;
-    const int kc = p.kc_blocks;
-    const SmemPlan plan = make_plan(MT, GROUP, kc, NS);
-    const int stages = plan.stages;
+    // K ranges in whole groups, so that a group never straddles two ranks.
+    const int nu = p.K / kKBlock / BPG;
+    const int b_begin = (int)((long long)nu * rank / S) * BPG;
+    const int b_end = (int)((long long)nu * (rank + 1) / S) * BPG;
+    const int nstage = (b_end - b_begin + kBPS - 1) / kBPS;
+    const int kc = p.kc_blocks;  // a multiple of kBPS unless it covers the whole range
+    const SmemPlan plan = make_plan(p.M, MT, GROUP, kc, NS, STAGES);
 
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + plan.bar_off);
-    uint64_t *empty = full + stages;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + stages);
+    uint64_t *empty = full + STAGES;
+    uint64_t *abar = empty + STAGES;  // activation chunk landed
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(abar + 1);
+    __half *sA = reinterpret_cast<__half *>(smem + plan.a_off);
+    const uint32_t blk_bytes = (uint32_t)R * 32u;  // one (tile, k-block) chunk
+
+    // Activations [M][c0*64, c1*64) of a chunk: one bulk copy per token row.
+    auto issue_activations = [&](int c0, int c1) {
+        const uint32_t row_bytes = (uint32_t)(c1 - c0) * kKBlock * 2u;
+        ptx::mbar_arrive_expect_tx(abar, (uint32_t)p.M * row_bytes);
+        for (int m = 0; m < p.M; ++m)
+            ptx::bulk_g2s(sA + (size_t)m * plan.a_stride, p.A + (size_t)m * p.K + (size_t)c0 * kKBlock, row_bytes,
+                          abar);
+    };
     if (tid == 0) {
-        for (int s = 0; s < stages; ++s) {
+        for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], kConsumerWarps);
+            ptx::mbar_init(&empty[s], CW);
         }
+        ptx::mbar_init(abar, 1);
         *abort_flag = 0;
         ptx::mbar_init_fence();
     }
+    // Metadata of the first chunk, first batch of 8 groups per row: the loads are
+    // issued before the barrier that releases the weight stream, so they are
+    // ahead of it in the memory system (they are latency-critical, it is not).
+    constexpr int RPT = (NS * kTileRows + NC - 1) / NC;  // metadata rows per consumer thread
+    const int zpstride = (p.G + 1) / 2;
+    constexpr int PREB = RPT == 1 ? 2 : 1;  // prefetched batches of 8 groups
+    float pre_s[RPT][PREB][8];
+    uint32_t pre_z[RPT][PREB][8];
+    auto load_meta_batch = [&](int row_set, int grp_first, int count, float (&sv)[8], uint32_t (&zb)[8]) {
+        const int w = row_set / kTileRows, row = row_set % kTileRows;
+        const int n = n0 + row;
+        const uint8_t *zrow = p.w[w].zp ? p.w[w].zp + (size_t)n * zpstride : nullptr;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int grp = grp_first + u;
+            sv[u] = 0.f;
+            zb[u] = 0x88u;
+            if (u < count && row < R) {
+                const size_t si = (size_t)n * p.G + grp;
+                sv[u] = p.scale_f32 ? __ldg(reinterpret_cast<const float *>(p.w[w].scales) + si)
+                                    : __half2float(__ldg(reinterpret_cast<const __half *>(p.w[w].scales) + si));
+                if (zrow) zb[u] = __ldg(zrow + (grp >> 1));
+            }
+        }
+    };
+    const int grp_first0 = (b_begin * kKBlock) / GROUP;
+    const int ng_first0 = ((min(b_begin + kc, b_end) - b_begin) * kKBlock) / GROUP;
+    if (warp < CW) {
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int rs = tid + NC * r;
+            if (rs < NS * kTileRows) {
+#pragma unroll
+                for (int bt = 0; bt < PREB; ++bt)
+                    load_meta_batch(rs, grp_first0 + 8 * bt, min(8, ng_first0 - 8 * bt), pre_s[r][bt], pre_z[r][bt]);
+            }
+        }
+    }
     __syncthreads();
 
-    const uint32_t chunk_bytes = (uint32_t)R * 32u;
-    float *P = reinterpret_cast<float *>(smem);  // partial tile, valid after the main loop
-    const size_t set_floats = (size_t)8 * MT * kPartStride;
-
-    if (warp == kConsumerWarps) {
+    if (warp == CW) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int it = 0;
-            for (; it < nblk; ++it) {
-                const int s = it % stages;
-                const uint32_t ph = (uint32_t)(it / stages) & 1u;
+            issue_activations(b_begin, min(b_begin + kc, b_end));
+            const uint64_t stream_policy = ptx::policy_evict_first();
+            int st = 0;
+            for (; st < nstage; ++st) {
+                const int s = st % STAGES;
+                const uint32_t ph = (uint32_t)(st / STAGES) & 1u;
                 if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err)) break;
-                ptx::mbar_arrive_expect_tx(&full[s], NS * chunk_bytes);
-                const size_t off = chunk_offset(n0, p.N, p.K, b_begin + it);
+                const int b0 = b_begin + st * kBPS;
+                const uint32_t bytes = blk_bytes * (uint32_t)min(kBPS, b_end - b0);
+                ptx::mbar_arrive_expect_tx(&full[s], NS * bytes);
+                const size_t off = chunk_offset(n0, p.N, p.K, b0);
 #pragma unroll
                 for (int w = 0; w < NS; ++w)
-                    ptx::bulk_g2s(smem + (size_t)(s * NS + w) * kChunkMax, p.w[w].q_rep + off, chunk_bytes,
-                                  &full[s]);
+                    ptx::bulk_g2s_hint(smem + (size_t)(s * NS + w) * kStageSet, p.w[w].q_rep + off, bytes, &full[s],
+                                       stream_policy);
             }
             if (*abort_flag) {
                 // Let the copies already issued land before the CTA can exit.
                 volatile int no_abort = 0;
-                for (int s = 0; s < stages && s < it; ++s) {
-                    const int last = s + ((it - 1 - s) / stages) * stages;
-                    ptx::mbar_wait(&full[s], (uint32_t)(last / stages) & 1u, &no_abort, nullptr,
-                                   200000000ull);
+                for (int s = 0; s < STAGES && s < st; ++s) {
+                    const int last = s + ((st - 1 - s) / STAGES) * STAGES;
+                    ptx::mbar_wait(&full[s], (uint32_t)(last / STAGES) & 1u, &no_abort, nullptr, 200000000ull);
                 }
+                ptx::mbar_wait(abar, 0u, &no_abort, nullptr, 200000000ull);
             }
         }
         __syncwarp();
@@ -151,174 +239,232 @@ __global__ void __launch_bounds__(kSmallMThreads, (MinBlocks<MT, SWIGLU>::value)
         // ------------------------------------------------------------ consumers
         const int g = lane >> 2, t = lane & 3;
         const int slot = 4 * g + ((t + (g >> 1)) & 3);  // lane slot of fragment (g, t)
-        const int cw = warp;                             // sub-tile of this warp
-        const bool active = cw < nsub;
-        const int rg = cw * kSubRows + g;                // tile row of fragment half 0
-        const int zpstride = (p.G + 1) / 2;
+        for (int i = tid; i < plan.a_stride; i += NC) sA[(size_t)p.M * plan.a_stride + i] = __float2half(0.f);
+        bool sub_ok[SUBT];
+#pragma unroll
+        for (int u = 0; u < SUBT; ++u) sub_ok[u] = warp * SUBT + u < nsub;
+        // Shared-memory row of token 8*mt + g (padding tokens read the zero row).
+        int arow[MT];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) arow[mt] = min(8 * mt + g, p.M) * plan.a_stride;
+        const float2 *meta0 = reinterpret_cast<const float2 *>(smem + plan.meta_off);
+        const int meta_set = (int)(plan.meta_set_bytes / 8);
+        int mrow[SUBT][2];
+#pragma unroll
+        for (int u = 0; u < SUBT; ++u) {
+            const int rg = (warp * SUBT + u) * kSubRows + g;
+            mrow[u][0] = rg * plan.ng;
+            mrow[u][1] = (rg + 8) * plan.ng;
+        }
 
-        __half *sA = reinterpret_cast<__half *>(smem + plan.a_off);
-        float *sSc = reinterpret_cast<float *>(smem + plan.meta_off);
-        const size_t meta_words = plan.meta_set_bytes / 4;  // per set: ng*128 floats + ng*128 words
-
-        for (int m = p.M; m < 8 * MT; ++m)
-            for (int i = tid; i < plan.a_stride; i += kConsumers)
-                sA[(size_t)m * plan.a_stride + i] = __float2half(0.f);
-
-        float acc[NS][MT][4];
+        float acc[NS][SUBT][MT][4];
 #pragma unroll
         for (int w = 0; w < NS; ++w)
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
+            for (int u = 0; u < SUBT; ++u)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc[w][mt][i] = 0.f;
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[w][u][mt][i] = 0.f;
 
         bool aborted = false;
         for (int c0 = b_begin; c0 < b_end; c0 += kc) {
             const int c1 = min(c0 + kc, b_end);
             const int grp0 = (c0 * kKBlock) / GROUP;
-            const int ng = ((c1 * kKBlock - 1) / GROUP) - grp0 + 1;
-            ptx::named_bar_sync(1, kConsumers);  // previous chunk consumed
-            {   // activations [M][c0*64, c1*64): 16-byte async copies
-                const int per_row = (c1 - c0) * kKBlock / 8;
-                for (int i = tid; i < p.M * per_row; i += kConsumers) {
-                    const int m = i / per_row, q = i % per_row;
-                    ptx::cp_async16(sA + (size_t)m * plan.a_stride + q * 8,
-                                    p.A + (size_t)m * p.K + (size_t)c0 * kKBlock + q * 8);
-                }
+            const int ng = ((c1 - c0) * kKBlock) / GROUP;
+            ptx::named_bar_sync(1, NC);  // previous chunk consumed
+            if (tid == 0 && c0 != b_begin) {  // later chunks: generic reads of sA before the async writes
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue_activations(c0, c1);
             }
-            // Scales (as float) and zero points (as half2 of 1024 + zp): all loads
-            // of a batch are issued before any is used.
+            // Per row and group: (s / f, (s / f)(1024 + f zp)), f = 16 for the second
+            // row of each 16-row fragment block. One row per thread, loads batched.
 #pragma unroll
-            for (int w = 0; w < NS; ++w) {
-                float *sc = sSc + w * meta_words;
-                uint32_t *zz = reinterpret_cast<uint32_t *>(sc) + (size_t)kTileRows * plan.ng;
-                const uint8_t *zpg = p.w[w].zp;
-                const int total = R * ng;
-                for (int base = 0; base < total; base += kConsumers * 8) {
+            for (int r = 0; r < RPT; ++r) {
+                const int rs = tid + NC * r;
+                if (rs >= NS * kTileRows) continue;
+                const int w = rs / kTileRows, row = rs % kTileRows;
+                if (row >= R) continue;
+                float2 *meta = reinterpret_cast<float2 *>(smem + plan.meta_off + w * plan.meta_set_bytes) +
+                               (size_t)row * plan.ng;
+                const float f = ((row >> 3) & 1) ? 16.f : 1.f;
+                for (int gb = 0; gb < ng; gb += 8) {
                     float sv[8];
                     uint32_t zb[8];
+                    if (c0 == b_begin && gb < 8 * PREB) {
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int i = base + tid + kConsumers * u;
-                        sv[u] = 0.f;
-                        zb[u] = 0x88u;
-                        if (i < total) {
-                            const int row = i / ng, gi = i % ng;
-                            const int grp = grp0 + gi;
-                            if (grp < p.G) {
-                                const size_t si = (size_t)(n0 + row) * p.G + grp;
-                                sv[u] = p.scale_f32
-                                            ? __ldg(reinterpret_cast<const float *>(p.w[w].scales) + si)
-                                            : __half2float(__ldg(reinterpret_cast<const __half *>(p.w[w].scales) + si));
-                                if (zpg) zb[u] = __ldg(zpg + (size_t)(n0 + row) * zpstride + (grp >> 1));
-                            }
+                        for (int u = 0; u < 8; ++u) {
+                            sv[u] = gb == 0 ? pre_s[r][0][u] : pre_s[r][PREB - 1][u];
+                            zb[u] = gb == 0 ? pre_z[r][0][u] : pre_z[r][PREB - 1][u];
                         }
+                    } else {
+                        load_meta_batch(rs, grp0 + gb, min(8, ng - gb), sv, zb);
                     }
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
-                        const int i = base + tid + kConsumers * u;
-                        if (i < total) {
-                            const int row = i / ng, gi = i % ng;
-                            const uint32_t zv = ((grp0 + gi) & 1) ? (zb[u] >> 4) : (zb[u] & 0xFu);
-                            const uint32_t h = 0x6400u + zv;  // fp16 bits of 1024 + zp
-                            sc[row * plan.ng + gi] = sv[u];
-                            zz[row * plan.ng + gi] = h | (h << 16);
+                        if (gb + u < ng) {
+                            const int grp = grp0 + gb + u;
+                            const float zv = (float)((grp & 1) ? (zb[u] >> 4) : (zb[u] & 0xFu));
+                            const float sf = sv[u] / f;
+                            meta[gb + u] = make_float2(sf, sf * (1024.f + f * zv));
                         }
                     }
                 }
             }
-            ptx::cp_async_wait_all();
-            ptx::named_bar_sync(1, kConsumers);
+            const int chunk_idx = (c0 - b_begin) / kc;
+            if (!aborted && !ptx::mbar_wait(abar, (uint32_t)chunk_idx & 1u, abort_flag, p.err)) aborted = true;
+            // Group activation sums A_g[token] of this chunk (fp32 over the fp16
+            // values), one (group, token) per thread with independent loads.
+            {
+                float *gs = reinterpret_cast<float *>(smem + plan.gsum_off);
+                for (int i = tid; i < ng * 8 * MT; i += NC) {
+                    const int gi = i / (8 * MT), m = i % (8 * MT);
+                    float v0 = 0.f, v1 = 0.f;
+                    if (m < p.M && !aborted) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(sA + (size_t)m * plan.a_stride + gi * GROUP);
+#pragma unroll
+                        for (int q = 0; q < GROUP / 8; ++q) {
+                            const uint4 x = src[q];
+                            const __half2 *h = reinterpret_cast<const __half2 *>(&x);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f2 = __half22float2(h[e]);
+                                v0 += f2.x;
+                                v1 += f2.y;
+                            }
+                        }
+                    }
+                    gs[i] = v0 + v1;
+                }
+            }
+            ptx::named_bar_sync(1, NC);
 
-            for (int b = c0; b < c1; ++b) {
-                const int it = b - b_begin;
-                const int s = it % stages;
-                const uint32_t ph = (uint32_t)(it / stages) & 1u;
+            float accg[NS][SUBT][MT][4];  // partial sum of the current group
+            const int st0 = (c0 - b_begin) / kBPS, st1 = (c1 - b_begin + kBPS - 1) / kBPS;
+            for (int st = st0; st < st1; ++st) {
+                const int s = st % STAGES;
+                const uint32_t ph = (uint32_t)(st / STAGES) & 1u;
                 if (!aborted && !ptx::mbar_wait(&full[s], ph, abort_flag, p.err)) aborted = true;
                 if (aborted) continue;
-                uint4 wv[NS];
-                if (active) {
-#pragma unroll
-                    for (int w = 0; w < NS; ++w)
-                        wv[w] = *reinterpret_cast<const uint4 *>(smem + (size_t)(s * NS + w) * kChunkMax +
-                                                                 cw * kSubBytes + slot * 16);
-                }
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&empty[s]);
-                if (!active) continue;
-
-                const int kl = (b - c0) * kKBlock;
-                float accg[NS][MT][4];
-                uint32_t zz0[NS], zz1[NS];
-                float sc0[NS], sc1[NS];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (j % SPF == 0) {
-                        const int gi = ((b * kKBlock + 16 * j) / GROUP) - grp0;
-#pragma unroll
-                        for (int w = 0; w < NS; ++w) {
-                            const float *sc = sSc + w * meta_words;
-                            const uint32_t *zz = reinterpret_cast<const uint32_t *>(sc) + (size_t)kTileRows * plan.ng;
-                            zz0[w] = zz[rg * plan.ng + gi];
-                            zz1[w] = zz[(rg + 8) * plan.ng + gi];
-                            sc0[w] = sc[rg * plan.ng + gi];
-                            sc1[w] = sc[(rg + 8) * plan.ng + gi];
-                        }
-                    }
-                    // Activation fragment of each token tile: k = 16j + 4t .. +3.
-                    uint32_t bfr[MT][2];
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        const uint2 v = *reinterpret_cast<const uint2 *>(
-                            sA + (size_t)(8 * mt + g) * plan.a_stride + kl + 16 * j + 4 * t);
-                        bfr[mt][0] = v.x;
-                        bfr[mt][1] = v.y;
-                    }
-#pragma unroll
-                    for (int w = 0; w < NS; ++w) {
-                        const uint32_t word = (&wv[w].x)[j];
-                        uint32_t a[4];
-                        a[0] = sub_f16x2((word & 0x000F000Fu) | 0x64006400u, zz0[w]);
-                        a[1] = sub_f16x2(((word >> 4) & 0x000F000Fu) | 0x64006400u, zz1[w]);
-                        a[2] = sub_f16x2(((word >> 8) & 0x000F000Fu) | 0x64006400u, zz0[w]);
-                        a[3] = sub_f16x2(((word >> 12) & 0x000F000Fu) | 0x64006400u, zz1[w]);
+                const unsigned char *ring = smem + (size_t)s * NS * kStageSet;
+                const int bs = b_begin + st * kBPS;  // first k-block of the stage
+                static_for<0, kBPS>([&](auto ic) {
+                    constexpr int i = decltype(ic)::value;
+                    const int b = bs + i;
+                    if (b >= c1) return;
+                    uint4 wv[NS][SUBT];
+                    static_for<0, NS>([&](auto wc) {
+                        constexpr int w = decltype(wc)::value;
+                        static_for<0, SUBT>([&](auto uc) {
+                            constexpr int u = decltype(uc)::value;
+                            wv[w][u] = *reinterpret_cast<const uint4 *>(ring + w * kStageSet + i * blk_bytes +
+                                                                       (warp * SUBT + u) * kSubBytes + slot * 16);
+                        });
+                    });
+                    const __half *ablk = sA + (b - c0) * kKBlock + 4 * t;
+                    static_for<0, 4>([&](auto jc) {
+                        constexpr int j = decltype(jc)::value;
+                        constexpr int step = i * 4 + j;  // k16 step within the stage
+                        // Activation fragment of each token tile: k = 16j + 4t .. +3.
+                        uint32_t bfr[MT][2];
 #pragma unroll
                         for (int mt = 0; mt < MT; ++mt) {
-                            if (j % SPF == 0) {
-                                const float z4[4] = {0.f, 0.f, 0.f, 0.f};
-                                mma_16816(accg[w][mt], a, bfr[mt][0], bfr[mt][1], z4);
-                            } else {
-                                mma_16816(accg[w][mt], a, bfr[mt][0], bfr[mt][1], accg[w][mt]);
-                            }
+                            const uint2 v = *reinterpret_cast<const uint2 *>(ablk + arow[mt] + 16 * j);
+                            bfr[mt][0] = v.x;
+                            bfr[mt][1] = v.y;
                         }
-                        if (j % SPF == SPF - 1) {
+                        static_for<0, NS>([&](auto wc) {
+                            constexpr int w = decltype(wc)::value;
+                            static_for<0, SUBT>([&](auto uc) {
+                                constexpr int u = decltype(uc)::value;
+                                const uint32_t word = j == 0 ? wv[w][u].x : j == 1 ? wv[w][u].y
+                                                    : j == 2 ? wv[w][u].z : wv[w][u].w;
+                                const uint32_t w8 = word >> 8;
+                                uint32_t a[4];
+                                a[0] = lop_or<0x000F000Fu>(word);  // row g,   k 4t+0/1: 1024 + q
+                                a[1] = lop_or<0x00F000F0u>(word);  // row g+8, k 4t+0/1: 1024 + 16 q
+                                a[2] = lop_or<0x000F000Fu>(w8);    // row g,   k 4t+2/3
+                                a[3] = lop_or<0x00F000F0u>(w8);    // row g+8, k 4t+2/3
 #pragma unroll
-                            for (int mt = 0; mt < MT; ++mt) {
-                                acc[w][mt][0] = fmaf(sc0[w], accg[w][mt][0], acc[w][mt][0]);
-                                acc[w][mt][1] = fmaf(sc0[w], accg[w][mt][1], acc[w][mt][1]);
-                                acc[w][mt][2] = fmaf(sc1[w], accg[w][mt][2], acc[w][mt][2]);
-                                acc[w][mt][3] = fmaf(sc1[w], accg[w][mt][3], acc[w][mt][3]);
-                            }
+                                for (int mt = 0; mt < MT; ++mt) {
+                                    if constexpr (step % SPG == 0) {
+                                        const float z4[4] = {0.f, 0.f, 0.f, 0.f};
+                                        mma_16816(accg[w][u][mt], a, bfr[mt][0], bfr[mt][1], z4);
+                                    } else {
+                                        mma_16816(accg[w][u][mt], a, bfr[mt][0], bfr[mt][1], accg[w][u][mt]);
+                                    }
+                                }
+                            });
+                        });
+                        if constexpr (step % SPG == SPG - 1) {
+                            // Group complete: acc += (s / f) * acc_g.
+                            const int gi = (b * kKBlock + 16 * j) / GROUP - grp0;
+                            static_for<0, NS>([&](auto wc) {
+                                constexpr int w = decltype(wc)::value;
+                                static_for<0, SUBT>([&](auto uc) {
+                                    constexpr int u = decltype(uc)::value;
+                                    const float s0 = meta0[w * meta_set + mrow[u][0] + gi].x;
+                                    const float s1 = meta0[w * meta_set + mrow[u][1] + gi].x;
+#pragma unroll
+                                    for (int mt = 0; mt < MT; ++mt) {
+                                        float *ac = acc[w][u][mt];
+                                        const float *ag = accg[w][u][mt];
+                                        ac[0] = fmaf(s0, ag[0], ac[0]);
+                                        ac[1] = fmaf(s0, ag[1], ac[1]);
+                                        ac[2] = fmaf(s1, ag[2], ac[2]);
+                                        ac[3] = fmaf(s1, ag[3], ac[3]);
+                                    }
+                                });
+                            });
                         }
+                    });
+                });
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&empty[s]);
+            }
+            // Offset and zero-point term of this chunk: acc -= sum_g (s/f)(1024 + f zp) A_g.
+            {
+                const float *gsum = reinterpret_cast<const float *>(smem + plan.gsum_off);
+                for (int gi = 0; gi < ng; ++gi) {
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        const float2 ag = *reinterpret_cast<const float2 *>(gsum + gi * 8 * MT + 8 * mt + 2 * t);
+#pragma unroll
+                        for (int w = 0; w < NS; ++w)
+#pragma unroll
+                            for (int u = 0; u < SUBT; ++u) {
+                                const float c0v = meta0[w * meta_set + mrow[u][0] + gi].y;
+                                const float c1v = meta0[w * meta_set + mrow[u][1] + gi].y;
+                                float *ac = acc[w][u][mt];
+                                ac[0] = fmaf(-c0v, ag.x, ac[0]);
+                                ac[1] = fmaf(-c0v, ag.y, ac[1]);
+                                ac[2] = fmaf(-c1v, ag.x, ac[2]);
+                                ac[3] = fmaf(-c1v, ag.y, ac[3]);
+                            }
                     }
                 }
             }
         }
 
-        // Partial tile -> shared memory as [set][token][row]; it overlays the ring
-        // and the staging area, which every consumer warp has finished with.
-        ptx::named_bar_sync(1, kConsumers);
-        if (active) {
+        // Partial tile -> shared memory as [set][token][row]; it overlays the ring,
+        // which every consumer warp has finished with (all copies have landed).
+        ptx::named_bar_sync(1, NC);
+        float *P = reinterpret_cast<float *>(smem);
+        const size_t set_floats = (size_t)8 * MT * kPartStride;
+#pragma unroll
+        for (int u = 0; u < SUBT; ++u) {
+            if (!sub_ok[u]) continue;
+            const int rg = (warp * SUBT + u) * kSubRows + g;
 #pragma unroll
             for (int w = 0; w < NS; ++w)
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
                     float *Pw = P + w * set_floats;
                     const int m0 = 8 * mt + 2 * t;
-                    Pw[(size_t)m0 * kPartStride + rg] = acc[w][mt][0];
-                    Pw[(size_t)(m0 + 1) * kPartStride + rg] = acc[w][mt][1];
-                    Pw[(size_t)m0 * kPartStride + rg + 8] = acc[w][mt][2];
-                    Pw[(size_t)(m0 + 1) * kPartStride + rg + 8] = acc[w][mt][3];
+                    Pw[(size_t)m0 * kPartStride + rg] = acc[w][u][mt][0];
+                    Pw[(size_t)(m0 + 1) * kPartStride + rg] = acc[w][u][mt][1];
+                    Pw[(size_t)m0 * kPartStride + rg + 8] = acc[w][u][mt][2];
+                    Pw[(size_t)(m0 + 1) * kPartStride + rg + 8] = acc[w][u][mt][3];
                 }
         }
     }
@@ -326,18 +472,25 @@ __global__ void __launch_bounds__(kSmallMThreads, (MinBlocks<MT, SWIGLU>::value)
     if (S > 1) ptx::cluster_sync(); else __syncthreads();
 
     // Rank r finalises rows [r*R/S, (r+1)*R/S): partials of ranks 0..S-1 summed in order.
-    if (tid < kConsumers) {
+    {
+        const float *P = reinterpret_cast<const float *>(smem);
+        const size_t set_floats = (size_t)8 * MT * kPartStride;
         const int lo = (int)((long long)R * rank / S), hi = (int)((long long)R * (rank + 1) / S);
         const int nr = hi - lo;
-        for (int i = tid; i < p.M * nr; i += kConsumers) {
+        for (int i = tid; i < p.M * nr; i += Sh::THREADS) {
             const int m = i / nr, row = lo + i % nr;
             float v[NS];
 #pragma unroll
             for (int w = 0; w < NS; ++w) {
                 const float *src = P + w * set_floats + (size_t)m * kPartStride + row;
                 if (S > 1) {
-                    float sum = ptx::ld_dsmem_f32(src, 0);
-                    for (int q = 1; q < S; ++q) sum += ptx::ld_dsmem_f32(src, (uint32_t)q);
+                    float part[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) part[q] = q < S ? ptx::ld_dsmem_f32(src, (uint32_t)q) : 0.f;
+                    float sum = part[0];
+#pragma unroll
+                    for (int q = 1; q < 8; ++q)
+                        if (q < S) sum += part[q];  // rank order: deterministic
                     v[w] = sum;
                 } else {
                     v[w] = *src;
@@ -351,19 +504,62 @@ __global__ void __launch_bounds__(kSmallMThreads, (MinBlocks<MT, SWIGLU>::value)
     if (S > 1) ptx::cluster_sync();  // keep shared memory alive until every peer has read it
 }
 
+constexpr int kMaxDynSmem = 227 * 1024;
+
+// Raise the kernel's dynamic shared-memory limit once per device.
 template <int GROUP, int MT, bool SWIGLU>
-cudaError_t launch_one(const SmallMParams &p, cudaStream_t s) {
-    const size_t smem = make_plan(MT, GROUP, p.kc_blocks, SWIGLU ? 2 : 1).total;
-    auto kern = smallm_kernel<GROUP, MT, SWIGLU>;
-    static size_t configured = 0;
-    if (smem > configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+cudaError_t configure() {
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && !done[dev]) {
+        e = cudaFuncSetAttribute(smallm_kernel<GROUP, MT, SWIGLU>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
         if (e != cudaSuccess) return e;
-        configured = smem;
+        done[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+// CTAs of a (1 x split) cluster launch that the device keeps resident at once.
+template <int GROUP, int MT, bool SWIGLU>
+int occupancy(size_t smem, int split) {
+    if (configure<GROUP, MT, SWIGLU>() != cudaSuccess) return 0;
+    int n = 0;
+    if (split <= 1) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, smallm_kernel<GROUP, MT, SWIGLU>,
+                                                          Shape<MT, SWIGLU>::THREADS, smem) != cudaSuccess)
+            return 0;
+        int dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        return n * sms;
     }
     cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1024, (unsigned)split, 1);
+    cfg.blockDim = dim3(Shape<MT, SWIGLU>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)split;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, smallm_kernel<GROUP, MT, SWIGLU>, &cfg) != cudaSuccess) return 0;
+    return n * split;
+}
+
+template <int GROUP, int MT, bool SWIGLU>
+cudaError_t launch_one(const SmallMParams &p, cudaStream_t s) {
+    const size_t smem = make_plan(p.M, MT, GROUP, p.kc_blocks, SWIGLU ? 2 : 1, Shape<MT, SWIGLU>::STAGES).total;
+    auto kern = smallm_kernel<GROUP, MT, SWIGLU>;
+    cudaError_t e = configure<GROUP, MT, SWIGLU>();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((p.N + kTileRows - 1) / kTileRows), (unsigned)p.split, 1);
-    cfg.blockDim = dim3(kSmallMThreads, 1, 1);
+    cfg.blockDim = dim3(Shape<MT, SWIGLU>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -374,6 +570,25 @@ cudaError_t launch_one(const SmallMParams &p, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = p.split > 1 ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int GROUP, bool SWIGLU>
+int occupancy_mt(int M, size_t smem, int split) {
+    const int mt = (M + 7) / 8;
+    if (mt <= 1) return occupancy<GROUP, 1, SWIGLU>(smem, split);
+    if (mt <= 2) return occupancy<GROUP, 2, SWIGLU>(smem, split);
+    if (mt <= 4) return occupancy<GROUP, 4, SWIGLU>(smem, split);
+    return occupancy<GROUP, 8, SWIGLU>(smem, split);
+}
+
+template <bool SWIGLU>
+int occupancy_group(int M, int group, size_t smem, int split) {
+    switch (group) {
+        case 16: return occupancy_mt<16, SWIGLU>(M, smem, split);
+        case 32: return occupancy_mt<32, SWIGLU>(M, smem, split);
+        case 64: return occupancy_mt<64, SWIGLU>(M, smem, split);
+        default: return occupancy_mt<128, SWIGLU>(M, smem, split);
+    }
 }
 
 template <int GROUP, bool SWIGLU>
@@ -400,24 +615,73 @@ int mt_of(int M) {
     return mt <= 1 ? 1 : mt <= 2 ? 2 : mt <= 4 ? 4 : 8;
 }
 
+int threads_of(int M, bool swiglu) {
+    const int mt = mt_of(M);
+    const int ns = swiglu ? 2 : 1;
+    const int subt = (mt * ns <= 2) ? 2 : 1;
+    return (8 / subt) * 32 + 32;
+}
+
 }  // namespace
 
 size_t smallm_smem_bytes(int M, int group, bool swiglu, int kc_blocks) {
-    return make_plan(mt_of(M), group, kc_blocks, swiglu ? 2 : 1).total;
+    return make_plan(M, mt_of(M), group, kc_blocks, swiglu ? 2 : 1, 2).total;
 }
 
-int smallm_ctas_per_sm(int M, bool swiglu) {
-    const int mt = mt_of(M);
-    return (mt * (swiglu ? 2 : 1) <= 4) ? 2 : 1;
-}
+int smallm_threads(int M, bool swiglu) { return threads_of(M, swiglu); }
 
-// Largest activation chunk (in k-blocks) that keeps one CTA's shared memory
-// within the budget for the resident CTAs per SM.
-int smallm_max_kc(int M, int group, bool swiglu) {
-    const size_t budget = smallm_ctas_per_sm(M, swiglu) == 2 ? 112 * 1024 : 220 * 1024;
-    int kc = 1;
-    while (kc < 1024 && smallm_smem_bytes(M, group, swiglu, kc + 1) <= budget) ++kc;
-    return kc;
+// Split (cluster size) and activation chunk for one shape. The choice maximises
+// the CTAs resident at once (bytes in flight) among grids that fit in one wave;
+// ties go to fewer activation chunks per CTA. A forced split only picks the chunk.
+SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k, int sm_count) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int, bool, int, int>, SmallMPlan> cache;
+    const auto key = std::make_tuple(M, N, K, group, swiglu, split_k, sm_count);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    const int bpg = group > kKBlock ? group / kKBlock : 1;  // k-blocks per group
+    const int nu = K / kKBlock / bpg;                       // K split unit: whole groups
+    const int n_tiles = (N + kTileRows - 1) / kTileRows;
+    SmallMPlan best{0, 0, 0, 0};
+    long long best_score = -1;
+    const int hi = split_k > 0 ? split_k : 8;
+    const int lo = split_k > 0 ? split_k : 1;
+    for (int split = hi; split >= lo; --split) {
+        if (split > nu) continue;
+        const int per_rank = (nu + split - 1) / split * bpg;
+        const int pf = kBPS;  // chunk boundaries stay on ring-stage boundaries
+        int prev_kc = -1;
+        for (int chunks = 1; chunks <= 8; ++chunks) {
+            int kc = (per_rank + chunks - 1) / chunks;
+            if (chunks > 1) kc = (kc + pf - 1) / pf * pf;
+            if (kc >= per_rank && chunks > 1) continue;
+            if (kc == prev_kc) continue;
+            prev_kc = kc;
+            const size_t smem = smallm_smem_bytes(M, group, swiglu, kc);
+            if (smem > (size_t)kMaxDynSmem) continue;
+            const int resident = swiglu ? occupancy_group<true>(M, group, smem, split)
+                                        : occupancy_group<false>(M, group, smem, split);
+            if (resident <= 0) continue;
+            const int occ = (resident + sm_count - 1) / sm_count;
+            const long long grid = (long long)n_tiles * split;
+            const long long slots = resident;
+            const long long waves = (grid + slots - 1) / slots;
+            // Concurrency per wave, discounted for extra waves and extra chunks.
+            const long long score = (grid / waves) * 64 / waves - (chunks - 1) * 2;
+            if (score > best_score) {
+                best_score = score;
+                best = SmallMPlan{split, (int)kc, (int)smem, occ};
+            }
+            if (waves == 1) break;  // more chunks only shrink the chunk further
+        }
+    }
+    if (best.split == 0) best = SmallMPlan{1, 1, (int)smallm_smem_bytes(M, group, swiglu, 1), 1};
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = best;
+    return best;
 }
 
 cudaError_t launch_smallm(const SmallMParams &p, int group, bool swiglu, cudaStream_t s) {

@@ -75,22 +75,11 @@ w4a16_status make_plan(int M, int N, int K, int group, int split_k, bool swiglu,
     const int smax = g_smallm_max;
     if (M <= smax) {
         p.path = W4A16_PATH_SMALL_M;
-        const int n_tiles = (N + kTileRows - 1) / kTileRows;
-        const int nb = K / kKBlock;
-        int split = split_k;
-        if (split == 0) {
-            // As many K ranks per tile as keep the whole grid resident in one wave.
-            const int per_sm = smallm_ctas_per_sm(M, swiglu);
-            split = (sm_count() * per_sm) / n_tiles;
-            if (split < 1) split = 1;
-            if (split > 8) split = 8;
-            while (split > 1 && nb / split < 2) --split;
-        }
-        if (split > nb) return W4A16_ERR_UNSUPPORTED;
-        p.split = split;
-        const int per_rank = (nb + split - 1) / split;
-        const int kc_max = smallm_max_kc(M, group, swiglu);
-        p.kc = per_rank < kc_max ? per_rank : kc_max;
+        if (split_k > K / (group > kKBlock ? group : kKBlock)) return W4A16_ERR_UNSUPPORTED;
+        const SmallMPlan sp = smallm_plan(M, N, K, group, swiglu, split_k, sm_count());
+        if (sp.split <= 0) return W4A16_ERR_UNSUPPORTED;
+        p.split = sp.split;
+        p.kc = sp.kc;
     } else {
         p.path = W4A16_PATH_TCGEN05;
         p.split = 1;

@@ -55,12 +55,18 @@ struct TcParams {
 cudaError_t launch_repack(const uint8_t *q, uint8_t *q_rep, int N, int K, cudaStream_t s);
 cudaError_t launch_smallm(const SmallMParams &p, int group, bool swiglu, cudaStream_t s);
 size_t smallm_smem_bytes(int M, int group, bool swiglu, int kc_blocks);
-int smallm_max_kc(int M, int group, bool swiglu);
-int smallm_ctas_per_sm(int M, bool swiglu);
+int smallm_threads(int M, bool swiglu);
+
+struct SmallMPlan {
+    int split;      // CTAs per row tile along K (cluster size, 1..8)
+    int kc;         // k-blocks per staged activation chunk
+    int smem;       // dynamic shared memory per CTA (bytes)
+    int per_sm;     // resident CTAs per SM at that shared-memory size
+};
+SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k, int sm_count);
 cudaError_t launch_silu_mul(const __half *G, const __half *U, __half *Y, size_t n,
                             cudaStream_t s);
 
-constexpr int kSmallMThreads = 288;  // 8 consumer warps (one sub-tile each) + 1 producer warp
 constexpr int kSmallMMaxM = 64;      // 8 token tiles of 8
 
 }  // namespace w4a16
