@@ -153,6 +153,32 @@ w4a16_status w4a16_gemm_swiglu(const uint16_t *A,
                                void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * Unfused SwiGLU (as w4a16_gemm_swiglu with fused = 0) for callers that cannot
+ * allocate device memory -- code inside another framework's memory pool, hot
+ * paths where an allocation that may synchronise the device is not allowed, or
+ * plug-ins that are handed only input and output buffers. No counterpart in the
+ * MatMulNBits pull request; this is a library convenience.
+ *   The fp16 gate and up intermediates (4*M*N bytes) live in a fixed array
+ *   compiled into the library, w4a16_swiglu_static_scratch_bytes() = 8 MiB,
+ *   one per GPU that loads the library, kept until the process exits. Shapes
+ *   whose 4*M*N exceeds it return W4A16_ERR_WORKSPACE and launch nothing.
+ *   The call allocates and frees nothing. Its first call on a device looks up the
+ *   array's device address (a runtime query, no allocation); make that first
+ *   call before any stream capture on that device.
+ *   Every call on a device shares the array, which keeps the last call's
+ *   intermediates: calls that can overlap on the GPU (different streams without
+ *   ordering between them) race and must not be issued that way. Nothing in the
+ *   array needs to start at zero.
+ *   Arguments, layouts and errors otherwise as w4a16_gemm_swiglu.
+ */
+size_t w4a16_swiglu_static_scratch_bytes(void);
+w4a16_status w4a16_gemm_swiglu_unfused_static(const uint16_t *A,
+                                              const uint8_t *qg_rep, const void *sg, const uint8_t *zg,
+                                              const uint8_t *qu_rep, const void *su, const uint8_t *zu,
+                                              w4a16_scale_dtype sdt, uint16_t *Y,
+                                              int M, int N, int K, int group, void *stream);
+
+/*
  * Tuning knobs (process-wide, not thread-safe; for tests and benchmarks).
  *   smallm_max  largest M routed to the small-M path (0 = default 64, max 64;
  *               -1 routes every M to the tensor-core path)

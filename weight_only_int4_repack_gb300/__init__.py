@@ -42,7 +42,7 @@ EXPORTS = (
     "w4a16_status_string", "w4a16_repacked_bytes", "w4a16_repack", "w4a16_unpack_host",
     "w4a16_gemm_workspace_bytes", "w4a16_gemm_plan", "w4a16_gemm",
     "w4a16_swiglu_workspace_bytes", "w4a16_gemm_swiglu", "w4a16_set_tuning",
-    "w4a16_device_error",
+    "w4a16_device_error", "w4a16_swiglu_static_scratch_bytes", "w4a16_gemm_swiglu_unfused_static",
 )
 
 _vp, _ci, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -59,6 +59,9 @@ _sig = {
                                 _ci, _ci, _ci, _ci, _ci, _vp, _sz, _vp]),
     "w4a16_set_tuning": (_ci, [_ci]),
     "w4a16_device_error": (_ci, [_vp]),
+    "w4a16_swiglu_static_scratch_bytes": (_sz, []),
+    "w4a16_gemm_swiglu_unfused_static": (_ci, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _vp,
+                                               _ci, _ci, _ci, _ci, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(lib, _name)
@@ -172,6 +175,27 @@ def w4a16_gemm_swiglu(A, qg_rep, sg, zg, qu_rep, su, zu, group: int, fused: bool
                                  _ptr(su), _ptr(zu), _scale_dtype(sg), _ptr(out), M, N, K, group,
                                  int(bool(fused)), _ptr(workspace), ws_bytes, _stream(stream)),
            "w4a16_gemm_swiglu")
+    return out
+
+
+def w4a16_swiglu_static_scratch_bytes() -> int:
+    return int(lib.w4a16_swiglu_static_scratch_bytes())
+
+
+def w4a16_gemm_swiglu_unfused_static(A, qg_rep, sg, zg, qu_rep, su, zu, group: int, out=None,
+                                     stream=None):
+    """Unfused SwiGLU whose intermediates live in the library's fixed device
+    array: for callers that cannot allocate device memory (see include/w4a16.h)."""
+    import torch
+    M, K = A.shape
+    N = sg.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    _check(lib.w4a16_gemm_swiglu_unfused_static(_ptr(A), _ptr(qg_rep), _ptr(sg), _ptr(zg),
+                                                _ptr(qu_rep), _ptr(su), _ptr(zu),
+                                                _scale_dtype(sg), _ptr(out), M, N, K, group,
+                                                _stream(stream)),
+           "w4a16_gemm_swiglu_unfused_static")
     return out
 
 
