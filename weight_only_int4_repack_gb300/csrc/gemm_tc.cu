@@ -1,0 +1,441 @@
+// Large-M W4A16 GEMM on the 5th-generation tensor cores (tcgen05, tensor memory).
+//
+// The MatMulNBits Marlin pull request (github.com/justinchuby/onnx-genai pull
+// 960, "What's landed") runs an SM80 mma.sync kernel for every M > 1. On sm_103a
+// the contraction at large M belongs on tcgen05, so this kernel is new:
+//   * roles are swapped: the dequantised weights are the MMA's A operand (M = 128
+//     weight rows per tile) held in tensor memory, and the activations are the B
+//     operand (N = T tokens, 16..256) staged by TMA with the 128-byte swizzle;
+//     D = W . A^T accumulates in fp32 in tensor memory;
+//   * a producer warp issues, per 64-k block, one TMA box of activations and one
+//     cp.async.bulk copy of the weight chunk (4 KB contiguous in the repacked
+//     layout) into a ring of shared-memory stages;
+//   * four dequant warps (one thread per weight row, the row's tensor-memory
+//     lane) read their row's 64 nibbles from the chunk (four conflict-free
+//     128-bit loads thanks to the layout's lane-slot rotation), form
+//     w = (q - zp) * s in fp16 (nibbles OR-ed into the mantissa of 1024, then one
+//     exact subtraction of 1024 + zp and one multiply by the scale) and store the
+//     32 packed columns with tcgen05.st;
+//   * one thread issues the four K=16 MMAs per block and commits them to the
+//     stage's "empty" barrier; after the last block a commit releases the
+//     epilogue (the same four warps), which reads the accumulator with tcgen05.ld
+//     and stores fp16 (for SwiGLU: silu(gate) * up from two accumulators).
+// Every mbarrier wait is bounded; on expiry the kernel records
+// W4A16_ERR_TIMEOUT, drains what it issued, frees its tensor memory and returns.
+#include <cudaTypedefs.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "ptx.cuh"
+#include "w4a16_internal.h"
+
+namespace w4a16 {
+namespace {
+
+constexpr int kThreads = 192;      // warp 0 producer, warp 1 MMA + TMEM, warps 2-5 dequant/epilogue
+constexpr int kDequantWarp0 = 2;
+constexpr int kTmemCols = 512;
+constexpr int kChunk = kTileRows * 32;  // 4 KB weight chunk per 64-k block
+
+template <bool SWIGLU>
+struct TcShape {
+    static constexpr int NS = SWIGLU ? 2 : 1;
+    static constexpr int TMAX = SWIGLU ? 128 : 256;  // tokens per tile (MMA N)
+    static constexpr int STAGES = 4;
+};
+
+// ------------------------------------------------------------------ tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(ptx::smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16, one CTA.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on `bar` once every tcgen05 operation this thread issued so far is complete.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     ptx::smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);          // start address
+    d |= (uint64_t)1u << 16;                           // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024u >> 4) << 32;                 // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1u << 46;                           // descriptor version for tcgen05
+    d |= (uint64_t)2u << 61;                           // layout: 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_f16(int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
+
+// Shared memory: [B stages (1024-aligned)] [W stages] [barriers] [tmem slot].
+struct TcSmem {
+    int T, stages, ns;
+    size_t b_stage, w_off, bar_off, total;
+};
+__host__ __device__ inline TcSmem tc_smem(int T, int stages, int ns) {
+    TcSmem p;
+    p.T = T;
+    p.stages = stages;
+    p.ns = ns;
+    p.b_stage = (size_t)T * 128;  // T token rows x 64 fp16
+    p.w_off = p.b_stage * stages;
+    p.bar_off = p.w_off + (size_t)stages * ns * kChunk;
+    p.total = p.bar_off + (size_t)(3 * stages + 2) * 8 + 16;
+    return p;
+}
+
+// Per-row metadata of k-block kb: for each k16 step j, half2 (1024 + zp) and half2 s.
+template <int GROUP>
+__device__ __forceinline__ void load_row_meta(const TcParams &p, int w, int n, int kb, uint32_t (&zz)[4],
+                                              uint32_t (&ss)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int grp = (kb * kKBlock + 16 * j) / GROUP;
+        const size_t si = (size_t)n * p.G + grp;
+        float s;
+        if (p.scale_f32) s = __ldg(reinterpret_cast<const float *>(p.w[w].scales) + si);
+        else s = __half2float(__ldg(reinterpret_cast<const __half *>(p.w[w].scales) + si));
+        uint32_t z = 8;
+        if (p.w[w].zp) {
+            const uint8_t zb = __ldg(p.w[w].zp + (size_t)n * ((p.G + 1) / 2) + (grp >> 1));
+            z = (grp & 1) ? (zb >> 4) : (zb & 0xFu);
+        }
+        const uint32_t zh = 0x6400u + z;  // fp16 bits of 1024 + zp
+        zz[j] = zh | (zh << 16);
+        const uint32_t sh = (uint32_t)__half_as_ushort(__float2half_rn(s));
+        ss[j] = sh | (sh << 16);
+    }
+}
+
+template <int GROUP, bool SWIGLU>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcParams p, int T) {
+    using Sh = TcShape<SWIGLU>;
+    constexpr int NS = Sh::NS, STAGES = Sh::STAGES;
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // The B stages need 1024-byte alignment (128-byte swizzle atoms).
+    unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const TcSmem L = tc_smem(T, STAGES, NS);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
+    uint64_t *empty = full + STAGES;
+    uint64_t *afull = empty + STAGES;
+    uint64_t *accfull = afull + STAGES;
+    uint64_t *drain = accfull + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int m0 = blockIdx.x * T;
+    const int n0 = blockIdx.y * kTileRows;
+    const int R = min(kTileRows, p.N - n0);
+    const int nkb = p.K / kKBlock;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&afull[s], 128);
+        }
+        ptx::mbar_init(accfull, 1);
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0;
+        ptx::mbar_init_fence();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // Tensor-memory columns: accumulators (T per set), then STAGES x NS x 32 A columns.
+    const uint32_t acc_col = 0;
+    const uint32_t a_col0 = (uint32_t)(NS * T);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t stream_policy = ptx::policy_evict_first();
+            int kb = 0;
+            for (; kb < nkb; ++kb) {
+                const int s = kb % STAGES;
+                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+                if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err)) break;
+                const uint32_t wbytes = (uint32_t)R * 32u;
+                ptx::mbar_arrive_expect_tx(&full[s], (uint32_t)L.b_stage + NS * wbytes);
+                ptx::tma_load_2d(smem + (size_t)s * L.b_stage, &tmap_a, kb * kKBlock, m0, &full[s]);
+                const size_t off = chunk_offset(n0, p.N, p.K, kb);
+#pragma unroll
+                for (int w = 0; w < NS; ++w)
+                    ptx::bulk_g2s_hint(smem + L.w_off + (size_t)(s * NS + w) * kChunk, p.w[w].q_rep + off, wbytes,
+                                       &full[s], stream_policy);
+            }
+            if (*abort_flag) {  // let issued copies land before the CTA can exit
+                volatile int no_abort = 0;
+                for (int s = 0; s < STAGES && s < kb; ++s) {
+                    const int last = s + ((kb - 1 - s) / STAGES) * STAGES;
+                    ptx::mbar_wait(&full[s], (uint32_t)(last / STAGES) & 1u, &no_abort, nullptr, 200000000ull);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(T);
+            int kb = 0;
+            for (; kb < nkb; ++kb) {
+                const int s = kb % STAGES;
+                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+                if (!ptx::mbar_wait(&full[s], ph, abort_flag, p.err)) break;
+                if (!ptx::mbar_wait(&afull[s], ph, abort_flag, p.err)) break;
+                tc_fence_after();
+                const uint32_t b_base = ptx::smem_u32(smem + (size_t)s * L.b_stage);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint64_t bdesc = smem_desc_sw128(b_base + 32u * j);  // k16 step j: +32 bytes
+#pragma unroll
+                    for (int w = 0; w < NS; ++w)
+                        tc_mma(tmem + acc_col + (uint32_t)(w * T), tmem + a_col0 + (uint32_t)((s * NS + w) * 32 + 8 * j),
+                               bdesc, idesc, (kb > 0 || j > 0) ? 1u : 0u);
+                }
+                tc_commit(&empty[s]);  // frees the shared-memory stage and the A columns
+            }
+            if (kb == nkb) {
+                tc_commit(accfull);
+            } else {  // aborted: wait (bounded) for the MMAs already issued
+                tc_commit(drain);
+                volatile int no_abort = 0;
+                ptx::mbar_wait(drain, 0u, &no_abort, nullptr, 200000000ull);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ dequant, then epilogue
+        const int q = warp & 3;              // tensor-memory lane quarter of this warp
+        const int r = q * 32 + lane;         // weight row in the tile (= tensor-memory lane)
+        const int n = n0 + r;
+        const bool row_ok = r < R;
+        const int sub = r >> 4, g = r & 7, h = (r >> 3) & 1;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const int sh0 = 4 * h, sh1 = 4 * h + 8;  // nibble pairs (e0,e1) and (e2,e3) of this row
+        uint32_t zz[NS][4], ss[NS][4];
+        if (row_ok) {
+#pragma unroll
+            for (int w = 0; w < NS; ++w) load_row_meta<GROUP>(p, w, n, 0, zz[w], ss[w]);
+        }
+        bool aborted = false;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % STAGES;
+            const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+            if (!aborted && !ptx::mbar_wait(&full[s], ph, abort_flag, p.err)) aborted = true;
+            if (aborted) break;
+            // Next block's metadata, loaded early (it is used one block later).
+            uint32_t zzn[NS][4], ssn[NS][4];
+            if (row_ok && kb + 1 < nkb) {
+#pragma unroll
+                for (int w = 0; w < NS; ++w) load_row_meta<GROUP>(p, w, n, kb + 1, zzn[w], ssn[w]);
+            }
+#pragma unroll
+            for (int w = 0; w < NS; ++w) {
+                uint32_t col[32];
+                if (row_ok) {
+                    const unsigned char *chunk = smem + L.w_off + (size_t)(s * NS + w) * kChunk + sub * kSubBytes;
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(chunk + (4 * g + ((t + (g >> 1)) & 3)) * 16);
+                        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t lo = ((words[j] >> sh0) & 0x000F000Fu) | 0x64006400u;  // k 16j+4t+0/1
+                            const uint32_t hi = ((words[j] >> sh1) & 0x000F000Fu) | 0x64006400u;  // k 16j+4t+2/3
+                            col[8 * j + 2 * t] = hmul2(hsub2(lo, zz[w][j]), ss[w][j]);
+                            col[8 * j + 2 * t + 1] = hmul2(hsub2(hi, zz[w][j]), ss[w][j]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) col[c] = 0u;
+                }
+                tmem_st32(tmem + lane_base + a_col0 + (uint32_t)((s * NS + w) * 32), col);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            ptx::mbar_arrive(&afull[s]);
+            if (kb + 1 < nkb) {
+#pragma unroll
+                for (int w = 0; w < NS; ++w)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        zz[w][j] = zzn[w][j];
+                        ss[w][j] = ssn[w][j];
+                    }
+            }
+        }
+        // Epilogue: D[row r][token] -> Y[m0 + token][n].
+        if (!aborted && ptx::mbar_wait(accfull, 0u, abort_flag, p.err)) {
+            tc_fence_after();
+            for (int c0 = 0; c0 < T; c0 += 32) {
+                uint32_t v[32], u[32];
+                tmem_ld32(tmem + lane_base + acc_col + (uint32_t)c0, v);
+                if constexpr (SWIGLU) tmem_ld32(tmem + lane_base + acc_col + (uint32_t)(T + c0), u);
+                tmem_wait_ld();
+                if (row_ok) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int m = m0 + c0 + i;
+                        if (m < p.M) {
+                            float y = __uint_as_float(v[i]);
+                            if constexpr (SWIGLU) y = silu_f32(y) * __uint_as_float(u[i]);
+                            p.Y[(size_t)m * p.N + n] = __float2half_rn(y);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// TMA map over A [M][K] fp16: boxes of 64 k x T tokens, 128-byte swizzle, zero fill.
+bool make_tmap_a(CUtensorMap *map, const __half *A, int M, int K, int T) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kKBlock, (cuuint32_t)T};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(A), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int GROUP, bool SWIGLU>
+cudaError_t launch_tc_one(const TcParams &p, int T, cudaStream_t s) {
+    using Sh = TcShape<SWIGLU>;
+    CUtensorMap map;
+    if (!make_tmap_a(&map, p.A, p.M, p.K, T)) return cudaErrorInvalidValue;
+    const TcSmem L = tc_smem(T, Sh::STAGES, Sh::NS);
+    // One CTA per SM: the kernel takes all 512 tensor-memory columns.
+    const size_t smem = (L.total + 1024 > 120 * 1024) ? L.total + 1024 : 120 * 1024;
+    auto kern = tc_kernel<GROUP, SWIGLU>;
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    dim3 grid((unsigned)((p.M + T - 1) / T), (unsigned)((p.N + kTileRows - 1) / kTileRows), 1);
+    kern<<<grid, kThreads, smem, s>>>(map, p, T);
+    return cudaGetLastError();
+}
+
+template <bool SWIGLU>
+cudaError_t launch_tc_group(const TcParams &p, int group, int T, cudaStream_t s) {
+    switch (group) {
+        case 16: return launch_tc_one<16, SWIGLU>(p, T, s);
+        case 32: return launch_tc_one<32, SWIGLU>(p, T, s);
+        case 64: return launch_tc_one<64, SWIGLU>(p, T, s);
+        default: return launch_tc_one<128, SWIGLU>(p, T, s);
+    }
+}
+
+}  // namespace
+
+// Tokens per tile: the whole M rounded up to 16 when it fits, else the maximum.
+int tc_tile_tokens(int M, bool swiglu) {
+    const int tmax = swiglu ? TcShape<true>::TMAX : TcShape<false>::TMAX;
+    const int t = (M + 15) / 16 * 16;
+    return t < tmax ? t : tmax;
+}
+
+cudaError_t launch_tc(const TcParams &p, int group, bool swiglu, cudaStream_t s) {
+    const int T = tc_tile_tokens(p.M, swiglu);
+    return swiglu ? launch_tc_group<true>(p, group, T, s) : launch_tc_group<false>(p, group, T, s);
+}
+
+}  // namespace w4a16

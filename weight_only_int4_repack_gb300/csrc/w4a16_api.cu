@@ -84,7 +84,6 @@ w4a16_status make_plan(int M, int N, int K, int group, int split_k, bool swiglu,
         p.path = W4A16_PATH_TCGEN05;
         p.split = 1;
         p.kc = 0;
-        return W4A16_ERR_UNSUPPORTED;  // tensor-core path not built in this version
     }
     *out = p;
     return W4A16_OK;
@@ -219,6 +218,19 @@ static w4a16_status gemm_impl(const uint16_t *A, const WeightSet *ws_sets, int n
     Plan plan;
     w4a16_status st = make_plan(M, N, K, group, split_k, nsets == 2, &plan);
     if (st != W4A16_OK) return st;
+    unsigned int *err = device_error_ptr();
+    if (!err) return W4A16_ERR_CUDA;
+    if (plan.path == W4A16_PATH_TCGEN05) {
+        TcParams t{};
+        t.A = reinterpret_cast<const __half *>(A);
+        t.w[0] = ws_sets[0];
+        t.w[1] = nsets == 2 ? ws_sets[1] : ws_sets[0];
+        t.Y = reinterpret_cast<__half *>(Y);
+        t.M = M; t.N = N; t.K = K; t.G = K / group;
+        t.scale_f32 = sdt == W4A16_SCALE_F32;
+        t.err = err;
+        return from_cuda(launch_tc(t, group, nsets == 2, stream));
+    }
     SmallMParams p{};
     p.A = reinterpret_cast<const __half *>(A);
     p.w[0] = ws_sets[0];
@@ -228,8 +240,7 @@ static w4a16_status gemm_impl(const uint16_t *A, const WeightSet *ws_sets, int n
     p.scale_f32 = sdt == W4A16_SCALE_F32;
     p.split = plan.split;
     p.kc_blocks = plan.kc;
-    p.err = device_error_ptr();
-    if (!p.err) return W4A16_ERR_CUDA;
+    p.err = err;
     return from_cuda(launch_smallm(p, group, nsets == 2, stream));
 }
 

@@ -64,6 +64,8 @@ struct SmallMPlan {
     int per_sm;     // resident CTAs per SM at that shared-memory size
 };
 SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k, int sm_count);
+cudaError_t launch_tc(const TcParams &p, int group, bool swiglu, cudaStream_t s);
+int tc_tile_tokens(int M, bool swiglu);
 cudaError_t launch_silu_mul(const __half *G, const __half *U, __half *Y, size_t n,
                             cudaStream_t s);
 
