@@ -422,6 +422,55 @@ def extras(args, w4, torch, device, stream, l2):
     }
     del sets
 
+    # Tensor-core regime: MLP GEMM at larger M and the gate/up SwiGLU (fused vs unfused).
+    _, tf_peak, _ = load_peaks()
+    base = make_case(8, 13824, 5120, 128, seed=2)
+    rot = weights(base, copies_min=2)
+    rows = {}
+    for m in (128, 256, 1024, 4096):
+        A = torch.randn((m, 5120), device=device).half()
+        Yx = torch.empty((m, 13824), dtype=torch.float16, device=device)
+
+        def fn(i, A=A, Yx=Yx):
+            q, s_, z = rot[i % len(rot)]
+            w4.w4a16_gemm(A, q, s_, z, 128, out=Yx, stream=stream)
+        n = max(4, int(2000 / m))
+        us = time_calls(torch, stream, fn, n, reps=3)
+        tflops = 2 * m * 13824 * 5120 / us / 1e6
+        rows[f"M={m}"] = {"us": round(us, 2), "TFLOP/s": round(tflops, 1),
+                          "tensor_frac": round(tflops / tf_peak, 3),
+                          "path": ["small_m", "tcgen05"][w4.w4a16_gemm_plan(m, 13824, 5120, 128)[0]]}
+    res["mlp_large_m"] = rows
+    del rot
+
+    gc, uc = make_swiglu_case(8, 13824, 5120, 128, seed=4)
+    gq = w4.w4a16_repack(torch.from_numpy(gc.bq).to(device))
+    uq = w4.w4a16_repack(torch.from_numpy(uc.bq).to(device))
+    tens = [torch.from_numpy(x).to(device) for x in (gc.scales, gc.zp, uc.scales, uc.zp)]
+    rows = {}
+    for m in (256, 1024, 4096, 8192):
+        A = torch.randn((m, 5120), device=device).half()
+        Yx = torch.empty((m, 13824), dtype=torch.float16, device=device)
+        ws = torch.empty(w4.w4a16_swiglu_workspace_bytes(m, 13824, 5120, 128, 0), dtype=torch.uint8,
+                         device=device)
+        samples = {True: [], False: []}
+        n = max(2, int(1000 / m))
+        for _ in range(3):
+            for fused in (True, False):
+                def fn(i, fused=fused, A=A, Yx=Yx, ws=ws):
+                    w4.w4a16_gemm_swiglu(A, gq, tens[0], tens[1], uq, tens[2], tens[3], 128,
+                                         fused=fused, out=Yx, workspace=ws, stream=stream)
+                samples[fused].append(time_calls(torch, stream, fn, n))
+        fu, un = statistics.median(samples[True]), statistics.median(samples[False])
+        flops = 4 * m * 13824 * 5120
+        rows[f"M={m}"] = {"fused_us": round(fu, 1), "unfused_us": round(un, 1),
+                          "fused_TFLOP/s": round(flops / fu / 1e6, 1),
+                          "fused_tensor_frac": round(flops / fu / 1e6 / tf_peak, 3),
+                          "analytic_delta_bytes": 8 * m * 13824,
+                          "delta_note": "upper bound from shape, DRAM level"}
+        del ws
+    res["gate_up_swiglu"] = rows
+
     # Repack (one-time): read N*K/2 + write N*K/2 bytes.
     qsrc = torch.randint(0, 256, (13824, 2560), dtype=torch.uint8, device=device)
     qdst = torch.empty(13824 * 2560, dtype=torch.uint8, device=device)

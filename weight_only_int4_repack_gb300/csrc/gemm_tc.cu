@@ -10,16 +10,18 @@
 //   * a producer warp issues, per 64-k block, one TMA box of activations and one
 //     cp.async.bulk copy of the weight chunk (4 KB contiguous in the repacked
 //     layout) into a ring of shared-memory stages;
-//   * four dequant warps (one thread per weight row, the row's tensor-memory
-//     lane) read their row's 64 nibbles from the chunk (four conflict-free
-//     128-bit loads thanks to the layout's lane-slot rotation), form
-//     w = (q - zp) * s in fp16 (nibbles OR-ed into the mantissa of 1024, then one
-//     exact subtraction of 1024 + zp and one multiply by the scale) and store the
-//     32 packed columns with tcgen05.st;
+//   * eight dequant warps, two per tensor-memory lane quarter (one thread per
+//     weight row, i.e. per lane; each of the two covers half the k16 steps), read
+//     their row's nibbles from the chunk (conflict-free thanks to the layout's
+//     lane-slot rotation), form w = (q - zp) * s in fp16 (nibbles OR-ed into the
+//     mantissa of 1024, one exact subtraction of 1024 + zp, one multiply by the
+//     scale) and store 16 packed columns each with tcgen05.st;
+//   * the shared-memory ring (TMA latency) is deeper than the tensor-memory ring
+//     of A stages (capacity-limited); each has its own "empty" barrier;
 //   * one thread issues the four K=16 MMAs per block and commits them to the
-//     stage's "empty" barrier; after the last block a commit releases the
-//     epilogue (the same four warps), which reads the accumulator with tcgen05.ld
-//     and stores fp16 (for SwiGLU: silu(gate) * up from two accumulators).
+//     "empty" barriers; after the last block a commit releases the epilogue (the
+//     same eight warps), which reads the accumulator with tcgen05.ld and stores
+//     fp16 (for SwiGLU: silu(gate) * up from two accumulators).
 // Every mbarrier wait is bounded; on expiry the kernel records
 // W4A16_ERR_TIMEOUT, drains what it issued, frees its tensor memory and returns.
 #include <cudaTypedefs.h>
@@ -34,8 +36,7 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kThreads = 192;      // warp 0 producer, warp 1 MMA + TMEM, warps 2-5 dequant/epilogue
-constexpr int kDequantWarp0 = 2;
+constexpr int kThreads = 320;      // warp 0 producer, warp 1 MMA + TMEM, warps 2-9 dequant/epilogue
 constexpr int kTmemCols = 512;
 constexpr int kChunk = kTileRows * 32;  // 4 KB weight chunk per 64-k block
 
@@ -43,7 +44,8 @@ template <bool SWIGLU>
 struct TcShape {
     static constexpr int NS = SWIGLU ? 2 : 1;
     static constexpr int TMAX = SWIGLU ? 128 : 256;  // tokens per tile (MMA N)
-    static constexpr int STAGES = 4;
+    static constexpr int STAGES = SWIGLU ? 8 : 6;    // shared-memory ring (TMA in flight)
+    static constexpr int ASTAGES = SWIGLU ? 4 : 6;   // tensor-memory A stages: NS*T + ASTAGES*NS*32 <= 512
 };
 
 // ------------------------------------------------------------------ tcgen05
@@ -75,26 +77,22 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
 }
@@ -131,28 +129,35 @@ __device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)
 
 // Shared memory: [B stages (1024-aligned)] [W stages] [barriers] [tmem slot].
 struct TcSmem {
-    int T, stages, ns;
+    int T, stages, astages, ns;
     size_t b_stage, w_off, bar_off, total;
 };
-__host__ __device__ inline TcSmem tc_smem(int T, int stages, int ns) {
+__host__ __device__ inline TcSmem tc_smem(int T, int stages, int astages, int ns) {
     TcSmem p;
     p.T = T;
     p.stages = stages;
+    p.astages = astages;
     p.ns = ns;
     p.b_stage = (size_t)T * 128;  // T token rows x 64 fp16
     p.w_off = p.b_stage * stages;
     p.bar_off = p.w_off + (size_t)stages * ns * kChunk;
-    p.total = p.bar_off + (size_t)(3 * stages + 2) * 8 + 16;
+    p.total = p.bar_off + (size_t)(2 * stages + 2 * astages + 2) * 8 + 16;
     return p;
 }
 
-// Per-row metadata of k-block kb: for each k16 step j, half2 (1024 + zp) and half2 s.
+// Per-row metadata of k-block kb for the k16 steps j0, j0+1: half2 (1024 + zp)
+// and half2 s (one group when GROUP >= 32).
 template <int GROUP>
-__device__ __forceinline__ void load_row_meta(const TcParams &p, int w, int n, int kb, uint32_t (&zz)[4],
-                                              uint32_t (&ss)[4]) {
+__device__ __forceinline__ void load_row_meta(const TcParams &p, int w, int n, int kb, int j0, uint32_t (&zz)[2],
+                                              uint32_t (&ss)[2]) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int grp = (kb * kKBlock + 16 * j) / GROUP;
+    for (int jj = 0; jj < 2; ++jj) {
+        if (GROUP >= 32 && jj == 1) {
+            zz[1] = zz[0];
+            ss[1] = ss[0];
+            continue;
+        }
+        const int grp = (kb * kKBlock + 16 * (j0 + jj)) / GROUP;
         const size_t si = (size_t)n * p.G + grp;
         float s;
         if (p.scale_f32) s = __ldg(reinterpret_cast<const float *>(p.w[w].scales) + si);
@@ -163,9 +168,9 @@ __device__ __forceinline__ void load_row_meta(const TcParams &p, int w, int n, i
             z = (grp & 1) ? (zb >> 4) : (zb & 0xFu);
         }
         const uint32_t zh = 0x6400u + z;  // fp16 bits of 1024 + zp
-        zz[j] = zh | (zh << 16);
+        zz[jj] = zh | (zh << 16);
         const uint32_t sh = (uint32_t)__half_as_ushort(__float2half_rn(s));
-        ss[j] = sh | (sh << 16);
+        ss[jj] = sh | (sh << 16);
     }
 }
 
@@ -173,16 +178,17 @@ template <int GROUP, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcParams p, int T) {
     using Sh = TcShape<SWIGLU>;
-    constexpr int NS = Sh::NS, STAGES = Sh::STAGES;
+    constexpr int NS = Sh::NS, STAGES = Sh::STAGES, ASTAGES = Sh::ASTAGES;
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // The B stages need 1024-byte alignment (128-byte swizzle atoms).
     unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const TcSmem L = tc_smem(T, STAGES, NS);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
-    uint64_t *empty = full + STAGES;
-    uint64_t *afull = empty + STAGES;
-    uint64_t *accfull = afull + STAGES;
+    const TcSmem L = tc_smem(T, STAGES, ASTAGES, NS);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);  // TMA + bulk copy landed
+    uint64_t *empty = full + STAGES;                                  // MMAs done with the smem stage
+    uint64_t *afull = empty + STAGES;                                 // A stage written to tensor memory
+    uint64_t *aempty = afull + ASTAGES;                               // MMAs done with the A stage
+    uint64_t *accfull = aempty + ASTAGES;
     uint64_t *drain = accfull + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -197,7 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
-            ptx::mbar_init(&afull[s], 128);
+        }
+        for (int s = 0; s < ASTAGES; ++s) {
+            ptx::mbar_init(&afull[s], 256);
+            ptx::mbar_init(&aempty[s], 1);
         }
         ptx::mbar_init(accfull, 1);
         ptx::mbar_init(drain, 1);
@@ -209,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // Tensor-memory columns: accumulators (T per set), then STAGES x NS x 32 A columns.
+    // Tensor-memory columns: accumulators (T per set), then ASTAGES x NS x 32 A columns.
     const uint32_t acc_col = 0;
     const uint32_t a_col0 = (uint32_t)(NS * T);
 
@@ -246,10 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = idesc_f16(T);
             int kb = 0;
             for (; kb < nkb; ++kb) {
-                const int s = kb % STAGES;
-                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+                const int s = kb % STAGES, sa = kb % ASTAGES;
+                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u, pa = (uint32_t)(kb / ASTAGES) & 1u;
                 if (!ptx::mbar_wait(&full[s], ph, abort_flag, p.err)) break;
-                if (!ptx::mbar_wait(&afull[s], ph, abort_flag, p.err)) break;
+                if (!ptx::mbar_wait(&afull[sa], pa, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t b_base = ptx::smem_u32(smem + (size_t)s * L.b_stage);
 #pragma unroll
@@ -257,10 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bdesc = smem_desc_sw128(b_base + 32u * j);  // k16 step j: +32 bytes
 #pragma unroll
                     for (int w = 0; w < NS; ++w)
-                        tc_mma(tmem + acc_col + (uint32_t)(w * T), tmem + a_col0 + (uint32_t)((s * NS + w) * 32 + 8 * j),
-                               bdesc, idesc, (kb > 0 || j > 0) ? 1u : 0u);
+                        tc_mma(tmem + acc_col + (uint32_t)(w * T),
+                               tmem + a_col0 + (uint32_t)((sa * NS + w) * 32 + 8 * j), bdesc, idesc,
+                               (kb > 0 || j > 0) ? 1u : 0u);
                 }
-                tc_commit(&empty[s]);  // frees the shared-memory stage and the A columns
+                tc_commit(&empty[s]);    // frees the shared-memory stage
+                tc_commit(&aempty[sa]);  // frees the tensor-memory A stage
             }
             if (kb == nkb) {
                 tc_commit(accfull);
@@ -274,76 +285,90 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ dequant, then epilogue
         const int q = warp & 3;              // tensor-memory lane quarter of this warp
+        const int hf = (warp - 2) >> 2;      // which half of the k16 steps (and of the epilogue columns)
         const int r = q * 32 + lane;         // weight row in the tile (= tensor-memory lane)
         const int n = n0 + r;
         const bool row_ok = r < R;
         const int sub = r >> 4, g = r & 7, h = (r >> 3) & 1;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int sh0 = 4 * h, sh1 = 4 * h + 8;  // nibble pairs (e0,e1) and (e2,e3) of this row
-        uint32_t zz[NS][4], ss[NS][4];
+        const int j0 = 2 * hf;                   // k16 steps j0, j0+1 of every block
+        uint32_t zz[NS][2], ss[NS][2];
         if (row_ok) {
 #pragma unroll
-            for (int w = 0; w < NS; ++w) load_row_meta<GROUP>(p, w, n, 0, zz[w], ss[w]);
+            for (int w = 0; w < NS; ++w) load_row_meta<GROUP>(p, w, n, 0, j0, zz[w], ss[w]);
         }
         bool aborted = false;
         for (int kb = 0; kb < nkb; ++kb) {
-            const int s = kb % STAGES;
-            const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+            const int s = kb % STAGES, sa = kb % ASTAGES;
+            const uint32_t ph = (uint32_t)(kb / STAGES) & 1u, pa = (uint32_t)(kb / ASTAGES) & 1u;
             if (!aborted && !ptx::mbar_wait(&full[s], ph, abort_flag, p.err)) aborted = true;
+            if (!aborted && !ptx::mbar_wait(&aempty[sa], pa ^ 1u, abort_flag, p.err)) aborted = true;
             if (aborted) break;
             // Next block's metadata, loaded early (it is used one block later).
-            uint32_t zzn[NS][4], ssn[NS][4];
+            uint32_t zzn[NS][2], ssn[NS][2];
             if (row_ok && kb + 1 < nkb) {
+                // With 128-wide groups, every other block continues the same group.
+                const bool same_group = GROUP > kKBlock && ((kb + 1) * kKBlock) / GROUP == (kb * kKBlock) / GROUP;
 #pragma unroll
-                for (int w = 0; w < NS; ++w) load_row_meta<GROUP>(p, w, n, kb + 1, zzn[w], ssn[w]);
+                for (int w = 0; w < NS; ++w) {
+                    if (same_group) {
+                        zzn[w][0] = zz[w][0]; zzn[w][1] = zz[w][1];
+                        ssn[w][0] = ss[w][0]; ssn[w][1] = ss[w][1];
+                    } else {
+                        load_row_meta<GROUP>(p, w, n, kb + 1, j0, zzn[w], ssn[w]);
+                    }
+                }
             }
 #pragma unroll
             for (int w = 0; w < NS; ++w) {
-                uint32_t col[32];
+                uint32_t col[16];
                 if (row_ok) {
                     const unsigned char *chunk = smem + L.w_off + (size_t)(s * NS + w) * kChunk + sub * kSubBytes;
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(chunk + (4 * g + ((t + (g >> 1)) & 3)) * 16);
-                        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+                        const uint2 v = *reinterpret_cast<const uint2 *>(
+                            chunk + (4 * g + ((t + (g >> 1)) & 3)) * 16 + 8 * hf);  // words j0, j0+1
+                        const uint32_t words[2] = {v.x, v.y};
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t lo = ((words[j] >> sh0) & 0x000F000Fu) | 0x64006400u;  // k 16j+4t+0/1
-                            const uint32_t hi = ((words[j] >> sh1) & 0x000F000Fu) | 0x64006400u;  // k 16j+4t+2/3
-                            col[8 * j + 2 * t] = hmul2(hsub2(lo, zz[w][j]), ss[w][j]);
-                            col[8 * j + 2 * t + 1] = hmul2(hsub2(hi, zz[w][j]), ss[w][j]);
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const uint32_t lo = ((words[jj] >> sh0) & 0x000F000Fu) | 0x64006400u;  // k +0/1
+                            const uint32_t hi = ((words[jj] >> sh1) & 0x000F000Fu) | 0x64006400u;  // k +2/3
+                            col[8 * jj + 2 * t] = hmul2(hsub2(lo, zz[w][jj]), ss[w][jj]);
+                            col[8 * jj + 2 * t + 1] = hmul2(hsub2(hi, zz[w][jj]), ss[w][jj]);
                         }
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) col[c] = 0u;
+                    for (int c = 0; c < 16; ++c) col[c] = 0u;
                 }
-                tmem_st32(tmem + lane_base + a_col0 + (uint32_t)((s * NS + w) * 32), col);
+                tmem_st16(tmem + lane_base + a_col0 + (uint32_t)((sa * NS + w) * 32 + 16 * hf), col);
             }
             tmem_wait_st();
             tc_fence_before();
-            ptx::mbar_arrive(&afull[s]);
+            ptx::mbar_arrive(&afull[sa]);
             if (kb + 1 < nkb) {
 #pragma unroll
                 for (int w = 0; w < NS; ++w)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        zz[w][j] = zzn[w][j];
-                        ss[w][j] = ssn[w][j];
+                    for (int jj = 0; jj < 2; ++jj) {
+                        zz[w][jj] = zzn[w][jj];
+                        ss[w][jj] = ssn[w][jj];
                     }
             }
         }
-        // Epilogue: D[row r][token] -> Y[m0 + token][n].
+        // Epilogue: D[row r][token] -> Y[m0 + token][n]; the two warps of a lane
+        // quarter take alternate 16-column chunks.
         if (!aborted && ptx::mbar_wait(accfull, 0u, abort_flag, p.err)) {
             tc_fence_after();
-            for (int c0 = 0; c0 < T; c0 += 32) {
-                uint32_t v[32], u[32];
-                tmem_ld32(tmem + lane_base + acc_col + (uint32_t)c0, v);
-                if constexpr (SWIGLU) tmem_ld32(tmem + lane_base + acc_col + (uint32_t)(T + c0), u);
+            for (int c0 = 16 * hf; c0 < T; c0 += 32) {
+                uint32_t v[16], u[16];
+                tmem_ld16(tmem + lane_base + acc_col + (uint32_t)c0, v);
+                if constexpr (SWIGLU) tmem_ld16(tmem + lane_base + acc_col + (uint32_t)(T + c0), u);
                 tmem_wait_ld();
                 if (row_ok) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
+                    for (int i = 0; i < 16; ++i) {
                         const int m = m0 + c0 + i;
                         if (m < p.M) {
                             float y = __uint_as_float(v[i]);
@@ -397,7 +422,7 @@ cudaError_t launch_tc_one(const TcParams &p, int T, cudaStream_t s) {
     using Sh = TcShape<SWIGLU>;
     CUtensorMap map;
     if (!make_tmap_a(&map, p.A, p.M, p.K, T)) return cudaErrorInvalidValue;
-    const TcSmem L = tc_smem(T, Sh::STAGES, Sh::NS);
+    const TcSmem L = tc_smem(T, Sh::STAGES, Sh::ASTAGES, Sh::NS);
     // One CTA per SM: the kernel takes all 512 tensor-memory columns.
     const size_t smem = (L.total + 1024 > 120 * 1024) ? L.total + 1024 : 120 * 1024;
     auto kern = tc_kernel<GROUP, SWIGLU>;

@@ -71,13 +71,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
 #pragma unroll 1
-    while (true) {
+    for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > limit_ns) {
-            if (err) atomicExch(err, (unsigned int)W4A16_ERR_TIMEOUT);
-            *abort_flag = 1;
-            return false;
+        if ((it & 63u) == 0) {  // the abort flag and the clock are checked now and then
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > limit_ns) {
+                if (err) atomicExch(err, (unsigned int)W4A16_ERR_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
         }
     }
 }
