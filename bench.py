@@ -35,7 +35,9 @@ METRIC = "W4A16 GEMM us per call (HBM roofline at M<=8)"
 # DRAM traffic per launch of the small-M kernel from an ncu capture, keyed by a
 # hash of the kernel source it was taken on (reported as null once the source
 # changes). Filled from profiles/ summaries.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    "f11abaffb5b5b616": 36915968,  # dram read + write, profiles/smallm_kernel_mlp_m8_K5120_N13824_g128.md
+}
 
 
 def algorithmic_bytes(m, n, k, group, scale_bytes=2, asym=True):
@@ -55,7 +57,7 @@ def load_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("gemm_smallm.cu", "w4a16_internal.h"):
+    for f in ("gemm_smallm.cu", "ptx.cuh", "w4a16_internal.h"):
         with open(os.path.join(ROOT, "weight_only_int4_repack_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -480,6 +482,49 @@ def extras(args, w4, torch, device, stream, l2):
     return res
 
 
+SINGLE_CASES = {
+    # name: (M, N, K, group, kind) -- a few calls of one workload, for profilers
+    "mlp-m8": (8, 13824, 5120, 128, "gemm"),
+    "mlp-m1": (1, 13824, 5120, 128, "gemm"),
+    "decode-m8": (8, 4096, 4096, 128, "gemm"),
+    "mlp-m1024": (1024, 13824, 5120, 128, "gemm"),
+    "mlp-m4096": (4096, 13824, 5120, 128, "gemm"),
+    "gateup-m1024-fused": (1024, 13824, 5120, 128, "swiglu-fused"),
+    "gateup-m1024-unfused": (1024, 13824, 5120, 128, "swiglu-unfused"),
+    "gateup-m8-fused": (8, 13824, 5120, 128, "swiglu-fused"),
+    "repack": (0, 13824, 5120, 128, "repack"),
+}
+
+
+def run_single(name, calls=3):
+    """Run `calls` calls of one workload (after building inputs) and exit; used
+    under ncu so that the profiled launches are the kernels of that workload."""
+    import torch
+    import weight_only_int4_repack_gb300 as w4
+    from w4a16_inputs import make_case, make_swiglu_case
+    M, N, K, group, kind = SINGLE_CASES[name]
+    dev = torch.device("cuda")
+    to = lambda a: torch.from_numpy(a).to(dev)  # noqa: E731
+    if kind == "repack":
+        q = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev)
+        for _ in range(calls):
+            w4.w4a16_repack(q)
+    elif kind == "gemm":
+        c = make_case(M, N, K, group, seed=SEED)
+        A, q, s, z = to(c.A), w4.w4a16_repack(to(c.bq)), to(c.scales), to(c.zp)
+        for _ in range(calls):
+            w4.w4a16_gemm(A, q, s, z, group)
+    else:
+        gc, uc = make_swiglu_case(M, N, K, group, seed=4)
+        args = (to(gc.A), w4.w4a16_repack(to(gc.bq)), to(gc.scales), to(gc.zp),
+                w4.w4a16_repack(to(uc.bq)), to(uc.scales), to(uc.zp), group)
+        for _ in range(calls):
+            w4.w4a16_gemm_swiglu(*args, fused=kind == "swiglu-fused")
+    torch.cuda.synchronize()
+    assert w4.w4a16_device_error() == 0
+    print(f"single {name}: {calls} calls ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -489,7 +534,12 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--single", choices=sorted(SINGLE_CASES),
+                    help="run a few calls of one workload and exit (for profilers)")
     args = ap.parse_args()
+    if args.single:
+        run_single(args.single)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

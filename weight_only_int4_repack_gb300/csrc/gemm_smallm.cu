@@ -33,6 +33,7 @@
 // CUDA-core FMA would need M FMAs per weight; at M = 8 that is about 0.57 G FMA
 // for K=5120, N=13824, more than the FP32 pipes finish in the HBM time of the
 // weight stream, so the contraction runs on the tensor cores.
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -48,6 +49,9 @@ constexpr int kPartStride = kTileRows + 4;          // floats per partial row (b
 constexpr int kBPS = 4;                             // k-blocks per ring stage
 constexpr int kStageSet = kTileRows * 32 * kBPS;    // 16 KB: one stage of one weight set
 
+// Ring stages of kStageSet bytes per weight set: 32 / 64 KB in flight per CTA.
+constexpr int kStages = 2;
+
 // Sub-tiles per consumer warp: two when the accumulators are small (shares the
 // activation fragments and the per-block overhead), else one.
 template <int MT, bool SWIGLU>
@@ -56,7 +60,7 @@ struct Shape {
     static constexpr int SUBT = (MT * NS <= 2) ? 2 : 1;
     static constexpr int CW = 8 / SUBT;             // consumer warps
     static constexpr int THREADS = CW * 32 + 32;    // + one producer warp
-    static constexpr int STAGES = 2;                // 32 / 64 KB of weights in flight per CTA
+    static constexpr int STAGES = kStages;
     static constexpr int MINB = SUBT == 2 ? 4 : (MT * NS <= 4 ? 2 : 1);
 };
 
@@ -625,7 +629,7 @@ int threads_of(int M, bool swiglu) {
 }  // namespace
 
 size_t smallm_smem_bytes(int M, int group, bool swiglu, int kc_blocks) {
-    return make_plan(M, mt_of(M), group, kc_blocks, swiglu ? 2 : 1, 2).total;
+    return make_plan(M, mt_of(M), group, kc_blocks, swiglu ? 2 : 1, kStages).total;
 }
 
 int smallm_threads(int M, bool swiglu) { return threads_of(M, swiglu); }
@@ -678,7 +682,11 @@ SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k,
             if (waves == 1) break;  // more chunks only shrink the chunk further
         }
     }
-    if (best.split == 0) best = SmallMPlan{1, 1, (int)smallm_smem_bytes(M, group, swiglu, 1), 1};
+    if (best.split == 0) {
+        // Nothing fit: the smallest chunk that is still whole ring stages and whole groups.
+        const int kc = std::min(K / kKBlock, std::max(kBPS, bpg));
+        best = SmallMPlan{1, kc, (int)smallm_smem_bytes(M, group, swiglu, kc), 1};
+    }
     std::lock_guard<std::mutex> lock(mu);
     cache[key] = best;
     return best;
