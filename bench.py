@@ -214,6 +214,7 @@ def run_ours(args):
         q, s_, z = rot[i % n_rot]
         w4.w4a16_gemm(A, q, s_, z, GROUP, out=Y, stream=s)
 
+    w4.w4a16_set_launch_overlap(args.launch_overlap)
     path, split = w4.w4a16_gemm_plan(M, N, K, GROUP)
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
@@ -301,7 +302,10 @@ def run_ours(args):
                    "l2_policy": f"weights rotate over {n_rot} copies "
                                 f"({n_rot * wbytes / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
                    "timing": f"CUDA graphs of {R} calls replayed back to back; CUDA events on the "
-                             "launching stream"},
+                             "launching stream",
+                   "launch_overlap": ("programmatic dependent launch: a call stages metadata and "
+                                      "streams weights while the previous call finishes"
+                                      if args.launch_overlap else "off")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": NCU_TRAFFIC.get(src_hash),
                      "peak_source": f"{peak_src} hbm_gbs", "bytes_per_call": bytes_alg,
@@ -312,6 +316,7 @@ def run_ours(args):
         "gpu_launches": args.steps,
     }
 
+    w4.w4a16_set_launch_overlap(False)
     if rank == 0 and not args.no_extras:
         out["extras"] = extras(args, w4, torch, device, stream, l2)
 
@@ -391,6 +396,30 @@ def extras(args, w4, torch, device, stream, l2):
                               "path": ["small_m", "tcgen05"][path]}
         res[name] = rows
         del rot
+
+    # Launch overlap (programmatic dependent launch) off vs on, interleaved samples.
+    base = make_case(32, 13824, 5120, 128, seed=2)
+    rot = weights(base)
+    ov = {}
+    for m in (1, 8, 32):
+        A = torch.from_numpy(base.A[:m].copy()).to(device)
+        Yx = torch.empty((m, 13824), dtype=torch.float16, device=device)
+
+        def fn(i, A=A, Yx=Yx):
+            q, s, z = rot[i % len(rot)]
+            w4.w4a16_gemm(A, q, s, z, 128, out=Yx, stream=stream)
+        smp = {False: [], True: []}
+        for _ in range(5):
+            for on in (False, True):
+                w4.w4a16_set_launch_overlap(on)
+                smp[on].append(time_calls(torch, stream, fn, 200))
+        w4.w4a16_set_launch_overlap(False)
+        b = algorithmic_bytes(m, 13824, 5120, 128)
+        off_us, on_us = statistics.median(smp[False]), statistics.median(smp[True])
+        ov[f"M={m}"] = {"off_us": round(off_us, 3), "on_us": round(on_us, 3),
+                        "on_hbm_frac": round(b / on_us / 1e3 / hbm_peak, 3)}
+    res["mlp_launch_overlap"] = ov
+    del rot
 
     # SwiGLU fused vs unfused at decode M (interleaved samples, same buffers).
     gc, uc = make_swiglu_case(8, 13824, 5120, 128, seed=4)
@@ -534,6 +563,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--launch-overlap", action="store_true",
+                    help="time the small-M calls as programmatic dependent launches")
     ap.add_argument("--single", choices=sorted(SINGLE_CASES),
                     help="run a few calls of one workload and exit (for profilers)")
     args = ap.parse_args()

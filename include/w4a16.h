@@ -186,6 +186,22 @@ w4a16_status w4a16_gemm_swiglu_unfused_static(const uint16_t *A,
 w4a16_status w4a16_set_tuning(int smallm_max);
 
 /*
+ * Overlap of consecutive small-M GEMM calls (process-wide, not thread-safe;
+ * default 0 = off). With enable = 1 each small-M launch is a programmatic
+ * dependent of the work before it on the stream: its CTAs may start while that
+ * work finishes, stage scales and zero points and start streaming q_rep, and
+ * wait for it to complete before they read A or write Y. So A and Y may be the
+ * previous call's output or input, as in a chain of layers, but q_rep, scales
+ * and zp must not be written by the work that directly precedes the call on
+ * the stream (weights loaded once and reused satisfy this; a w4a16_repack
+ * followed at once by a GEMM on the same weights does not). Results are
+ * identical with the switch on or off. The pages describe no such launch mode;
+ * it is a GB300 launch-latency measure.
+ * Returns W4A16_ERR_INVALID_ARG unless enable is 0 or 1.
+ */
+w4a16_status w4a16_set_launch_overlap(int enable);
+
+/*
  * Read and clear the device-side error word that bounded waits set when they
  * expire (W4A16_ERR_TIMEOUT) on the device current for the calling thread.
  * Synchronises `stream`. Returns W4A16_OK when no kernel reported an error.

@@ -116,6 +116,13 @@ def test_tuning_validation(w4):
     assert w4.lib.w4a16_set_tuning(0) == 0
 
 
+def test_launch_overlap_validation(w4):
+    assert w4.lib.w4a16_set_launch_overlap(2) == w4.W4A16_ERR_INVALID_ARG
+    assert w4.lib.w4a16_set_launch_overlap(-1) == w4.W4A16_ERR_INVALID_ARG
+    assert w4.lib.w4a16_set_launch_overlap(1) == 0
+    assert w4.lib.w4a16_set_launch_overlap(0) == 0
+
+
 def test_product_path_has_no_oracle_dependency():
     """The binding and the CUDA sources never reference the oracle."""
     pkg = os.path.join(ROOT, "weight_only_int4_repack_gb300")

@@ -41,7 +41,7 @@ W4A16_PATH_TCGEN05 = 1
 EXPORTS = (
     "w4a16_status_string", "w4a16_repacked_bytes", "w4a16_repack", "w4a16_unpack_host",
     "w4a16_gemm_workspace_bytes", "w4a16_gemm_plan", "w4a16_gemm",
-    "w4a16_swiglu_workspace_bytes", "w4a16_gemm_swiglu", "w4a16_set_tuning",
+    "w4a16_swiglu_workspace_bytes", "w4a16_gemm_swiglu", "w4a16_set_tuning", "w4a16_set_launch_overlap",
     "w4a16_device_error", "w4a16_swiglu_static_scratch_bytes", "w4a16_gemm_swiglu_unfused_static",
 )
 
@@ -58,6 +58,7 @@ _sig = {
     "w4a16_gemm_swiglu": (_ci, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _vp,
                                 _ci, _ci, _ci, _ci, _ci, _vp, _sz, _vp]),
     "w4a16_set_tuning": (_ci, [_ci]),
+    "w4a16_set_launch_overlap": (_ci, [_ci]),
     "w4a16_device_error": (_ci, [_vp]),
     "w4a16_swiglu_static_scratch_bytes": (_sz, []),
     "w4a16_gemm_swiglu_unfused_static": (_ci, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _vp,
@@ -201,6 +202,12 @@ def w4a16_gemm_swiglu_unfused_static(A, qg_rep, sg, zg, qu_rep, su, zu, group: i
 
 def w4a16_set_tuning(smallm_max: int) -> None:
     _check(lib.w4a16_set_tuning(smallm_max), "w4a16_set_tuning")
+
+
+def w4a16_set_launch_overlap(enable: bool) -> None:
+    """Let small-M GEMM calls start while the work before them finishes
+    (weights must not be written by that work); see include/w4a16.h."""
+    _check(lib.w4a16_set_launch_overlap(int(enable)), "w4a16_set_launch_overlap")
 
 
 def w4a16_device_error(stream=None) -> int:

@@ -208,16 +208,28 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
         }
     }
     __syncthreads();
+    ptx::grid_dep_launch();
 
     if (warp == CW) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            issue_activations(b_begin, min(b_begin + kc, b_end));
+            // A may be the previous kernel's output: it is read only after the
+            // wait on that kernel. Weights, scales and zero points are not, so as
+            // a programmatic dependent the first ring stages go out before it.
+            const int pre = p.overlap ? min(STAGES, nstage) : 0;
+            bool a_issued = false;
+            auto start_activations = [&]() {
+                ptx::grid_dep_wait();
+                issue_activations(b_begin, min(b_begin + kc, b_end));
+                a_issued = true;
+            };
+            if (pre == 0) start_activations();
             const uint64_t stream_policy = ptx::policy_evict_first();
             int st = 0;
             for (; st < nstage; ++st) {
                 const int s = st % STAGES;
                 const uint32_t ph = (uint32_t)(st / STAGES) & 1u;
+                if (st == pre && !a_issued) start_activations();
                 if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err)) break;
                 const int b0 = b_begin + st * kBPS;
                 const uint32_t bytes = blk_bytes * (uint32_t)min(kBPS, b_end - b0);
@@ -228,6 +240,7 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                     ptx::bulk_g2s_hint(smem + (size_t)(s * NS + w) * kStageSet, p.w[w].q_rep + off, bytes, &full[s],
                                        stream_policy);
             }
+            if (!a_issued && !*abort_flag) start_activations();
             if (*abort_flag) {
                 // Let the copies already issued land before the CTA can exit.
                 volatile int no_abort = 0;
@@ -235,7 +248,7 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                     const int last = s + ((st - 1 - s) / STAGES) * STAGES;
                     ptx::mbar_wait(&full[s], (uint32_t)(last / STAGES) & 1u, &no_abort, nullptr, 200000000ull);
                 }
-                ptx::mbar_wait(abar, 0u, &no_abort, nullptr, 200000000ull);
+                if (a_issued) ptx::mbar_wait(abar, 0u, &no_abort, nullptr, 200000000ull);
             }
         }
         __syncwarp();
@@ -474,6 +487,7 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
     }
 
     if (S > 1) ptx::cluster_sync(); else __syncthreads();
+    ptx::grid_dep_wait();  // Y may still be in use by the previous kernel
 
     // Rank r finalises rows [r*R/S, (r+1)*R/S): partials of ranks 0..S-1 summed in order.
     {
@@ -566,13 +580,22 @@ cudaError_t launch_one(const SmallMParams &p, cudaStream_t s) {
     cfg.blockDim = dim3(Shape<MT, SWIGLU>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = (unsigned)p.split;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (p.split > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = (unsigned)p.split;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (p.overlap) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = p.split > 1 ? 1 : 0;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

@@ -134,6 +134,14 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
 }
 
 // ---------------------------------------------------------------- cluster
+// Programmatic dependent launch. launch_dependents lets the next kernel on the
+// stream (launched with programmatic stream serialization) be scheduled once
+// every CTA of this grid has executed it; wait blocks until the grids this one
+// depends on have completed and their memory is visible. Without such a
+// dependency both are no-ops.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");

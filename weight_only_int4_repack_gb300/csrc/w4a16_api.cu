@@ -12,6 +12,7 @@ using namespace w4a16;
 namespace {
 
 int g_smallm_max = kSmallMMaxM;
+int g_launch_overlap = 0;  // small-M launches as programmatic dependents
 
 __device__ unsigned int g_device_error;  // set by bounded waits that expire
 
@@ -240,6 +241,7 @@ static w4a16_status gemm_impl(const uint16_t *A, const WeightSet *ws_sets, int n
     p.scale_f32 = sdt == W4A16_SCALE_F32;
     p.split = plan.split;
     p.kc_blocks = plan.kc;
+    p.overlap = g_launch_overlap;
     p.err = err;
     return from_cuda(launch_smallm(p, group, nsets == 2, stream));
 }
@@ -298,6 +300,12 @@ w4a16_status w4a16_gemm_swiglu(const uint16_t *A,
 w4a16_status w4a16_set_tuning(int smallm_max) {
     if (smallm_max < -1 || smallm_max > kSmallMMaxM) return W4A16_ERR_INVALID_ARG;
     g_smallm_max = smallm_max == 0 ? kSmallMMaxM : (smallm_max < 0 ? 0 : smallm_max);
+    return W4A16_OK;
+}
+
+w4a16_status w4a16_set_launch_overlap(int enable) {
+    if (enable != 0 && enable != 1) return W4A16_ERR_INVALID_ARG;
+    g_launch_overlap = enable;
     return W4A16_OK;
 }
 

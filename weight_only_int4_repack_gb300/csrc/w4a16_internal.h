@@ -39,6 +39,7 @@ struct SmallMParams {
     int scale_f32;
     int split;              // CTAs per row tile along K (cluster size)
     int kc_blocks;          // k-blocks per staged activation chunk
+    int overlap;            // launched as a programmatic dependent (weights read before the wait)
     unsigned int *err;      // device error word for bounded waits
 };
 
