@@ -102,9 +102,12 @@ def test_swiglu_large_m(gpu_lib, M, fused):
     check(Y1.float().cpu().double().numpy()[rows], ref, f"tc swiglu M={M} fused={fused}")
 
 
-@pytest.mark.parametrize("M,group", [(20, 32), (150, 16), (300, 128)])
-def test_swiglu_forced_tc(tc_only, M, group):
-    gc, uc = make_swiglu_case(M, 384, 512, group, seed=M)
+@pytest.mark.parametrize("M,N,group", [(20, 384, 32), (150, 384, 16), (300, 384, 128),
+                                       (100, 400, 64), (70, 208, 128), (33, 16, 16), (257, 80, 64)])
+def test_swiglu_forced_tc(tc_only, M, N, group):
+    # N = 400, 208, 80, 16: output halves of 64 columns that end inside a ragged
+    # 128-row tile of the repacked layout (or are the whole of one).
+    gc, uc = make_swiglu_case(M, N, 512, group, seed=M)
     ref = oracle.gemm_swiglu(gc.A, (gc.bq, gc.scales, gc.zp), (uc.bq, uc.scales, uc.zp), group)
     A = dev(gc.A)
     args = (A, tc_only.w4a16_repack(dev(gc.bq)), dev(gc.scales), dev(gc.zp),

@@ -21,7 +21,13 @@
 //   * one thread issues the four K=16 MMAs per block and commits them to the
 //     "empty" barriers; after the last block a commit releases the epilogue (the
 //     same eight warps), which reads the accumulator with tcgen05.ld and stores
-//     fp16 (for SwiGLU: silu(gate) * up from two accumulators).
+//     fp16;
+//   * fused SwiGLU keeps the plain GEMM's 256-token tile: a CTA owns 64 output
+//     columns, and its 128 MMA rows are those 64 gate rows followed by the same
+//     64 up rows (two 2 KB halves of the repacked chunks), so one accumulator
+//     holds both and every dequantised weight still serves 256 tokens. The
+//     epilogue pairs row r with row r + 64 through shared memory and stores
+//     silu(gate) * up.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // W4A16_ERR_TIMEOUT, drains what it issued, frees its tensor memory and returns.
 #include <cudaTypedefs.h>
@@ -40,12 +46,11 @@ constexpr int kThreads = 320;      // warp 0 producer, warp 1 MMA + TMEM, warps 
 constexpr int kTmemCols = 512;
 constexpr int kChunk = kTileRows * 32;  // 4 KB weight chunk per 64-k block
 
-template <bool SWIGLU>
 struct TcShape {
-    static constexpr int NS = SWIGLU ? 2 : 1;
-    static constexpr int TMAX = SWIGLU ? 128 : 256;  // tokens per tile (MMA N)
-    static constexpr int STAGES = SWIGLU ? 8 : 6;    // shared-memory ring (TMA in flight)
-    static constexpr int ASTAGES = SWIGLU ? 4 : 6;   // tensor-memory A stages: NS*T + ASTAGES*NS*32 <= 512
+    static constexpr int NS = 1;        // one accumulator (SwiGLU pairs its rows inside it)
+    static constexpr int TMAX = 256;    // tokens per tile (MMA N)
+    static constexpr int STAGES = 6;    // shared-memory ring (TMA in flight)
+    static constexpr int ASTAGES = 6;   // tensor-memory A stages: T + ASTAGES*32 <= 512
 };
 
 // ------------------------------------------------------------------ tcgen05
@@ -177,8 +182,9 @@ __device__ __forceinline__ void load_row_meta(const TcParams &p, int w, int n, i
 template <int GROUP, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcParams p, int T) {
-    using Sh = TcShape<SWIGLU>;
+    using Sh = TcShape;
     constexpr int NS = Sh::NS, STAGES = Sh::STAGES, ASTAGES = Sh::ASTAGES;
+    constexpr int COLS = SWIGLU ? 64 : kTileRows;  // output columns per CTA
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // The B stages need 1024-byte alignment (128-byte swizzle atoms).
@@ -195,8 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int m0 = blockIdx.x * T;
-    const int n0 = blockIdx.y * kTileRows;
-    const int R = min(kTileRows, p.N - n0);
+    const int n0 = blockIdx.y * COLS;               // first output column
+    const int R = min(COLS, p.N - n0);              // output columns of this CTA
+    const int nt0 = n0 / kTileRows * kTileRows;     // repacked tile holding them
+    const uint32_t half_off = (uint32_t)(n0 - nt0) / kSubRows * kSubBytes;  // SwiGLU: 2 KB into the chunk
     const int nkb = p.K / kKBlock;
 
     if (tid == 0) {
@@ -231,14 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = kb % STAGES;
                 const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
                 if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err)) break;
-                const uint32_t wbytes = (uint32_t)R * 32u;
-                ptx::mbar_arrive_expect_tx(&full[s], (uint32_t)L.b_stage + NS * wbytes);
+                const uint32_t wbytes = (uint32_t)R * 32u;  // this CTA's rows of one weight set
+                ptx::mbar_arrive_expect_tx(&full[s], (uint32_t)L.b_stage + (SWIGLU ? 2u : 1u) * wbytes);
                 ptx::tma_load_2d(smem + (size_t)s * L.b_stage, &tmap_a, kb * kKBlock, m0, &full[s]);
-                const size_t off = chunk_offset(n0, p.N, p.K, kb);
-#pragma unroll
-                for (int w = 0; w < NS; ++w)
-                    ptx::bulk_g2s_hint(smem + L.w_off + (size_t)(s * NS + w) * kChunk, p.w[w].q_rep + off, wbytes,
-                                       &full[s], stream_policy);
+                const size_t off = chunk_offset(nt0, p.N, p.K, kb) + half_off;
+                unsigned char *wdst = smem + L.w_off + (size_t)s * kChunk;
+                ptx::bulk_g2s_hint(wdst, p.w[0].q_rep + off, wbytes, &full[s], stream_policy);
+                if (SWIGLU)  // up rows in the second half of the slot
+                    ptx::bulk_g2s_hint(wdst + kChunk / 2, p.w[1].q_rep + off, wbytes, &full[s], stream_policy);
             }
             if (*abort_flag) {  // let issued copies land before the CTA can exit
                 volatile int no_abort = 0;
@@ -286,17 +294,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ dequant, then epilogue
         const int q = warp & 3;              // tensor-memory lane quarter of this warp
         const int hf = (warp - 2) >> 2;      // which half of the k16 steps (and of the epilogue columns)
-        const int r = q * 32 + lane;         // weight row in the tile (= tensor-memory lane)
-        const int n = n0 + r;
-        const bool row_ok = r < R;
-        const int sub = r >> 4, g = r & 7, h = (r >> 3) & 1;
+        const int r = q * 32 + lane;         // MMA row (= tensor-memory lane)
+        const int wset = SWIGLU ? r / COLS : 0;  // SwiGLU: rows 0-63 gate, 64-127 up
+        const int rr = r % COLS;             // output column within the CTA
+        const int n = n0 + rr;
+        const bool row_ok = rr < R;
+        const int sub = rr >> 4, g = r & 7, h = (r >> 3) & 1;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int sh0 = 4 * h, sh1 = 4 * h + 8;  // nibble pairs (e0,e1) and (e2,e3) of this row
         const int j0 = 2 * hf;                   // k16 steps j0, j0+1 of every block
         uint32_t zz[NS][2], ss[NS][2];
         if (row_ok) {
 #pragma unroll
-            for (int w = 0; w < NS; ++w) load_row_meta<GROUP>(p, w, n, 0, j0, zz[w], ss[w]);
+            for (int w = 0; w < NS; ++w) load_row_meta<GROUP>(p, wset + w, n, 0, j0, zz[w], ss[w]);
         }
         bool aborted = false;
         for (int kb = 0; kb < nkb; ++kb) {
@@ -316,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         zzn[w][0] = zz[w][0]; zzn[w][1] = zz[w][1];
                         ssn[w][0] = ss[w][0]; ssn[w][1] = ss[w][1];
                     } else {
-                        load_row_meta<GROUP>(p, w, n, kb + 1, j0, zzn[w], ssn[w]);
+                        load_row_meta<GROUP>(p, wset + w, n, kb + 1, j0, zzn[w], ssn[w]);
                     }
                 }
             }
@@ -324,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int w = 0; w < NS; ++w) {
                 uint32_t col[16];
                 if (row_ok) {
-                    const unsigned char *chunk = smem + L.w_off + (size_t)(s * NS + w) * kChunk + sub * kSubBytes;
+                    const unsigned char *chunk = smem + L.w_off + (size_t)(s * NS + w) * kChunk +
+                                                 wset * (kChunk / 2) + sub * kSubBytes;
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
                         const uint2 v = *reinterpret_cast<const uint2 *>(
@@ -359,24 +370,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Epilogue: D[row r][token] -> Y[m0 + token][n]; the two warps of a lane
         // quarter take alternate 16-column chunks.
-        if (!aborted && ptx::mbar_wait(accfull, 0u, abort_flag, p.err)) {
-            tc_fence_after();
-            for (int c0 = 16 * hf; c0 < T; c0 += 32) {
-                uint32_t v[16], u[16];
-                tmem_ld16(tmem + lane_base + acc_col + (uint32_t)c0, v);
-                if constexpr (SWIGLU) tmem_ld16(tmem + lane_base + acc_col + (uint32_t)(T + c0), u);
-                tmem_wait_ld();
-                if (row_ok) {
+        const bool acc_ok = !aborted && ptx::mbar_wait(accfull, 0u, abort_flag, p.err);
+        if constexpr (!SWIGLU) {
+            if (acc_ok) {
+                tc_fence_after();
+                for (int c0 = 16 * hf; c0 < T; c0 += 32) {
+                    uint32_t v[16];
+                    tmem_ld16(tmem + lane_base + acc_col + (uint32_t)c0, v);
+                    tmem_wait_ld();
+                    if (row_ok) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = m0 + c0 + i;
-                        if (m < p.M) {
-                            float y = __uint_as_float(v[i]);
-                            if constexpr (SWIGLU) y = silu_f32(y) * __uint_as_float(u[i]);
-                            p.Y[(size_t)m * p.N + n] = __float2half_rn(y);
+                        for (int i = 0; i < 16; ++i) {
+                            const int m = m0 + c0 + i;
+                            if (m < p.M) p.Y[(size_t)m * p.N + n] = __float2half_rn(__uint_as_float(v[i]));
                         }
                     }
                 }
+            }
+        } else {
+            // Each half of the epilogue warps (one per lane quarter) stages 16
+            // tokens x 128 rows in shared memory (the ring is idle once the last
+            // MMA has committed), then pairs gate row j with up row 64 + j.
+            // Every thread of the group runs the loop the same number of times,
+            // so the group barriers stay matched even after an abort.
+            constexpr int XS = kTileRows + 4;  // floats per staged token row
+            float *xb = reinterpret_cast<float *>(smem) + (size_t)hf * 16 * XS;
+            const int gt = (warp - 2 - 4 * hf) * 32 + lane;  // thread in the group, 0..127
+            if (acc_ok) tc_fence_after();
+            for (int c0 = 16 * hf; c0 < T; c0 += 32) {
+                uint32_t v[16];
+                tmem_ld16(tmem + lane_base + acc_col + (uint32_t)c0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) xb[i * XS + r] = __uint_as_float(v[i]);
+                ptx::named_bar_sync(1 + hf, 128);
+                if (acc_ok) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int idx = gt + 128 * k;
+                        const int i = idx / COLS, j = idx % COLS;
+                        const int m = m0 + c0 + i;
+                        if (m < p.M && j < R) {
+                            const float gv = xb[i * XS + j], uv = xb[i * XS + COLS + j];
+                            p.Y[(size_t)m * p.N + n0 + j] = __float2half_rn(silu_f32(gv) * uv);
+                        }
+                    }
+                }
+                ptx::named_bar_sync(1 + hf, 128);  // the buffer is rewritten next chunk
             }
         }
     }
@@ -419,7 +459,7 @@ bool make_tmap_a(CUtensorMap *map, const __half *A, int M, int K, int T) {
 
 template <int GROUP, bool SWIGLU>
 cudaError_t launch_tc_one(const TcParams &p, int T, cudaStream_t s) {
-    using Sh = TcShape<SWIGLU>;
+    using Sh = TcShape;
     CUtensorMap map;
     if (!make_tmap_a(&map, p.A, p.M, p.K, T)) return cudaErrorInvalidValue;
     const TcSmem L = tc_smem(T, Sh::STAGES, Sh::ASTAGES, Sh::NS);
@@ -434,7 +474,8 @@ cudaError_t launch_tc_one(const TcParams &p, int T, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    dim3 grid((unsigned)((p.M + T - 1) / T), (unsigned)((p.N + kTileRows - 1) / kTileRows), 1);
+    const int cols = SWIGLU ? 64 : kTileRows;  // output columns per CTA
+    dim3 grid((unsigned)((p.M + T - 1) / T), (unsigned)((p.N + cols - 1) / cols), 1);
     kern<<<grid, kThreads, smem, s>>>(map, p, T);
     return cudaGetLastError();
 }
@@ -453,7 +494,8 @@ cudaError_t launch_tc_group(const TcParams &p, int group, int T, cudaStream_t s)
 
 // Tokens per tile: the whole M rounded up to 16 when it fits, else the maximum.
 int tc_tile_tokens(int M, bool swiglu) {
-    const int tmax = swiglu ? TcShape<true>::TMAX : TcShape<false>::TMAX;
+    (void)swiglu;  // both modes use the same tile
+    const int tmax = TcShape::TMAX;
     const int t = (M + 15) / 16 * 16;
     return t < tmax ? t : tmax;
 }
