@@ -42,9 +42,13 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kThreads = 320;      // warp 0 producer, warp 1 MMA + TMEM, warps 2-9 dequant/epilogue
+constexpr int kSPW = 2;                      // k16 steps of a block that one dequant warp converts (2 measured faster than 1)
+constexpr int kDqParts = 4 / kSPW;           // dequant warps per tensor-memory lane quarter
+constexpr int kDqThreads = 128 * kDqParts;   // dequant / epilogue threads
+constexpr int kThreads = 64 + kDqThreads;    // warp 0 producer, warp 1 MMA + TMEM, then dequant/epilogue
 constexpr int kTmemCols = 512;
 constexpr int kChunk = kTileRows * 32;  // 4 KB weight chunk per 64-k block
+constexpr int kStageXS = kTileRows + 4;  // SwiGLU epilogue: floats per staged token row
 
 struct TcShape {
     static constexpr int NS = 1;        // one accumulator (SwiGLU pairs its rows inside it)
@@ -89,6 +93,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
         "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+    static_assert(N == 8 || N == 16, "8 or 16 columns");
+    if constexpr (N == 16) tmem_st16(taddr, r);
+    else tmem_st8(taddr, r);
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -146,20 +161,23 @@ __host__ __device__ inline TcSmem tc_smem(int T, int stages, int astages, int ns
     p.b_stage = (size_t)T * 128;  // T token rows x 64 fp16
     p.w_off = p.b_stage * stages;
     p.bar_off = p.w_off + (size_t)stages * ns * kChunk;
+    // The SwiGLU epilogue stages its tokens over the ring: keep the barriers above it.
+    const size_t stage_end = (size_t)kDqParts * 16 * kStageXS * 4;
+    if (p.bar_off < stage_end) p.bar_off = stage_end;
     p.total = p.bar_off + (size_t)(2 * stages + 2 * astages + 2) * 8 + 16;
     return p;
 }
 
-// Per-row metadata of k-block kb for the k16 steps j0, j0+1: half2 (1024 + zp)
-// and half2 s (one group when GROUP >= 32).
+// Per-row metadata of k-block kb for the k16 steps j0 .. j0+kSPW-1: half2
+// (1024 + zp) and half2 s (steps in one group share them).
 template <int GROUP>
-__device__ __forceinline__ void load_row_meta(const TcParams &p, int w, int n, int kb, int j0, uint32_t (&zz)[2],
-                                              uint32_t (&ss)[2]) {
+__device__ __forceinline__ void load_row_meta(const TcParams &p, int w, int n, int kb, int j0, uint32_t (&zz)[kSPW],
+                                              uint32_t (&ss)[kSPW]) {
 #pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
-        if (GROUP >= 32 && jj == 1) {
-            zz[1] = zz[0];
-            ss[1] = ss[0];
+    for (int jj = 0; jj < kSPW; ++jj) {
+        if (jj > 0 && (16 * (j0 + jj)) / GROUP == (16 * (j0 + jj - 1)) / GROUP) {
+            zz[jj] = zz[jj - 1];
+            ss[jj] = ss[jj - 1];
             continue;
         }
         const int grp = (kb * kKBlock + 16 * (j0 + jj)) / GROUP;
@@ -213,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&empty[s], 1);
         }
         for (int s = 0; s < ASTAGES; ++s) {
-            ptx::mbar_init(&afull[s], 256);
+            ptx::mbar_init(&afull[s], kDqThreads);
             ptx::mbar_init(&aempty[s], 1);
         }
         ptx::mbar_init(accfull, 1);
@@ -293,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ dequant, then epilogue
         const int q = warp & 3;              // tensor-memory lane quarter of this warp
-        const int hf = (warp - 2) >> 2;      // which half of the k16 steps (and of the epilogue columns)
+        const int hf = (warp - 2) >> 2;      // which k16 steps (and which epilogue column chunks)
         const int r = q * 32 + lane;         // MMA row (= tensor-memory lane)
         const int wset = SWIGLU ? r / COLS : 0;  // SwiGLU: rows 0-63 gate, 64-127 up
         const int rr = r % COLS;             // output column within the CTA
@@ -302,8 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sub = rr >> 4, g = r & 7, h = (r >> 3) & 1;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int sh0 = 4 * h, sh1 = 4 * h + 8;  // nibble pairs (e0,e1) and (e2,e3) of this row
-        const int j0 = 2 * hf;                   // k16 steps j0, j0+1 of every block
-        uint32_t zz[NS][2], ss[NS][2];
+        const int j0 = kSPW * hf;                // k16 steps j0 .. j0+kSPW-1 of every block
+        uint32_t zz[NS][kSPW], ss[NS][kSPW];
         if (row_ok) {
 #pragma unroll
             for (int w = 0; w < NS; ++w) load_row_meta<GROUP>(p, wset + w, n, 0, j0, zz[w], ss[w]);
@@ -316,15 +334,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!aborted && !ptx::mbar_wait(&aempty[sa], pa ^ 1u, abort_flag, p.err)) aborted = true;
             if (aborted) break;
             // Next block's metadata, loaded early (it is used one block later).
-            uint32_t zzn[NS][2], ssn[NS][2];
+            uint32_t zzn[NS][kSPW], ssn[NS][kSPW];
             if (row_ok && kb + 1 < nkb) {
                 // With 128-wide groups, every other block continues the same group.
                 const bool same_group = GROUP > kKBlock && ((kb + 1) * kKBlock) / GROUP == (kb * kKBlock) / GROUP;
 #pragma unroll
                 for (int w = 0; w < NS; ++w) {
                     if (same_group) {
-                        zzn[w][0] = zz[w][0]; zzn[w][1] = zz[w][1];
-                        ssn[w][0] = ss[w][0]; ssn[w][1] = ss[w][1];
+#pragma unroll
+                        for (int jj = 0; jj < kSPW; ++jj) {
+                            zzn[w][jj] = zz[w][jj];
+                            ssn[w][jj] = ss[w][jj];
+                        }
                     } else {
                         load_row_meta<GROUP>(p, wset + w, n, kb + 1, j0, zzn[w], ssn[w]);
                     }
@@ -332,17 +353,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int w = 0; w < NS; ++w) {
-                uint32_t col[16];
+                uint32_t col[8 * kSPW];
                 if (row_ok) {
                     const unsigned char *chunk = smem + L.w_off + (size_t)(s * NS + w) * kChunk +
                                                  wset * (kChunk / 2) + sub * kSubBytes;
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        const uint2 v = *reinterpret_cast<const uint2 *>(
-                            chunk + (4 * g + ((t + (g >> 1)) & 3)) * 16 + 8 * hf);  // words j0, j0+1
-                        const uint32_t words[2] = {v.x, v.y};
+                        // Words j0 .. j0+kSPW-1 of the row's lane slot for fragment column t.
+                        const unsigned char *slotp = chunk + (4 * g + ((t + (g >> 1)) & 3)) * 16 + 4 * j0;
+                        uint32_t words[kSPW];
+                        if constexpr (kSPW == 2) {
+                            const uint2 v = *reinterpret_cast<const uint2 *>(slotp);
+                            words[0] = v.x;
+                            words[kSPW - 1] = v.y;
+                        } else {
+                            words[0] = *reinterpret_cast<const uint32_t *>(slotp);
+                        }
 #pragma unroll
-                        for (int jj = 0; jj < 2; ++jj) {
+                        for (int jj = 0; jj < kSPW; ++jj) {
                             const uint32_t lo = ((words[jj] >> sh0) & 0x000F000Fu) | 0x64006400u;  // k +0/1
                             const uint32_t hi = ((words[jj] >> sh1) & 0x000F000Fu) | 0x64006400u;  // k +2/3
                             col[8 * jj + 2 * t] = hmul2(hsub2(lo, zz[w][jj]), ss[w][jj]);
@@ -351,9 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) col[c] = 0u;
+                    for (int c = 0; c < 8 * kSPW; ++c) col[c] = 0u;
                 }
-                tmem_st16(tmem + lane_base + a_col0 + (uint32_t)((sa * NS + w) * 32 + 16 * hf), col);
+                const uint32_t ta = tmem + lane_base + a_col0 + (uint32_t)((sa * NS + w) * 32 + 8 * kSPW * hf);
+                tmem_st_cols(ta, col);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -362,19 +391,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int w = 0; w < NS; ++w)
 #pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
+                    for (int jj = 0; jj < kSPW; ++jj) {
                         zz[w][jj] = zzn[w][jj];
                         ss[w][jj] = ssn[w][jj];
                     }
             }
         }
-        // Epilogue: D[row r][token] -> Y[m0 + token][n]; the two warps of a lane
+        // Epilogue: D[row r][token] -> Y[m0 + token][n]; the warps of a lane
         // quarter take alternate 16-column chunks.
         const bool acc_ok = !aborted && ptx::mbar_wait(accfull, 0u, abort_flag, p.err);
         if constexpr (!SWIGLU) {
             if (acc_ok) {
                 tc_fence_after();
-                for (int c0 = 16 * hf; c0 < T; c0 += 32) {
+                for (int c0 = 16 * hf; c0 < T; c0 += 16 * kDqParts) {
                     uint32_t v[16];
                     tmem_ld16(tmem + lane_base + acc_col + (uint32_t)c0, v);
                     tmem_wait_ld();
@@ -388,16 +417,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else {
-            // Each half of the epilogue warps (one per lane quarter) stages 16
-            // tokens x 128 rows in shared memory (the ring is idle once the last
-            // MMA has committed), then pairs gate row j with up row 64 + j.
+            // Each group of epilogue warps (one per lane quarter) stages 16 tokens
+            // x 128 rows in shared memory (the ring is idle once the last MMA has
+            // committed), then pairs gate row j with up row 64 + j.
             // Every thread of the group runs the loop the same number of times,
             // so the group barriers stay matched even after an abort.
-            constexpr int XS = kTileRows + 4;  // floats per staged token row
+            constexpr int XS = kStageXS;      // floats per staged token row
             float *xb = reinterpret_cast<float *>(smem) + (size_t)hf * 16 * XS;
             const int gt = (warp - 2 - 4 * hf) * 32 + lane;  // thread in the group, 0..127
             if (acc_ok) tc_fence_after();
-            for (int c0 = 16 * hf; c0 < T; c0 += 32) {
+            for (int c0 = 16 * hf; c0 < T; c0 += 16 * kDqParts) {
                 uint32_t v[16];
                 tmem_ld16(tmem + lane_base + acc_col + (uint32_t)c0, v);
                 tmem_wait_ld();
