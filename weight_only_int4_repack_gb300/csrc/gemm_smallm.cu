@@ -657,9 +657,13 @@ size_t smallm_smem_bytes(int M, int group, bool swiglu, int kc_blocks) {
 
 int smallm_threads(int M, bool swiglu) { return threads_of(M, swiglu); }
 
-// Split (cluster size) and activation chunk for one shape. The choice maximises
-// the CTAs resident at once (bytes in flight) among grids that fit in one wave;
-// ties go to fewer activation chunks per CTA. A forced split only picks the chunk.
+// Split (cluster size) and activation chunk for one shape. Among plans whose
+// grid is resident at once (one wave), the choice minimises the weight blocks
+// the busiest SM streams (CTAs per SM, rounded up, x blocks per CTA): measured
+// on GB300 at M=8 K=5120 N=13824, split 4 (432 CTAs, at most 3 per SM) beats
+// split 5 (540 CTAs, up to 4 per SM) by 9%. Ties go to the larger grid (more
+// bytes in flight), then to fewer activation chunks. Without a one-wave plan,
+// concurrency per wave decides. A forced split only picks the chunk.
 SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k, int sm_count) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int, int, bool, int, int>, SmallMPlan> cache;
@@ -673,7 +677,10 @@ SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k,
     const int nu = K / kKBlock / bpg;                       // K split unit: whole groups
     const int n_tiles = (N + kTileRows - 1) / kTileRows;
     SmallMPlan best{0, 0, 0, 0};
-    long long best_score = -1;
+    long long best_score = -1;              // multi-wave plans (used only if no one-wave plan)
+    SmallMPlan best1{0, 0, 0, 0};
+    long long best1_work = 0, best1_grid = 0;
+    int best1_chunks = 0;
     const int hi = split_k > 0 ? split_k : 8;
     const int lo = split_k > 0 ? split_k : 1;
     for (int split = hi; split >= lo; --split) {
@@ -696,15 +703,28 @@ SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k,
             const long long grid = (long long)n_tiles * split;
             const long long slots = resident;
             const long long waves = (grid + slots - 1) / slots;
+            if (waves == 1) {
+                const long long work = (grid + sm_count - 1) / sm_count * per_rank;  // busiest SM
+                const bool better = best1.split == 0 || work < best1_work ||
+                                    (work == best1_work && (grid > best1_grid ||
+                                                            (grid == best1_grid && chunks < best1_chunks)));
+                if (better) {
+                    best1 = SmallMPlan{split, (int)kc, (int)smem, occ};
+                    best1_work = work;
+                    best1_grid = grid;
+                    best1_chunks = chunks;
+                }
+                break;  // more chunks only shrink the chunk further
+            }
             // Concurrency per wave, discounted for extra waves and extra chunks.
             const long long score = (grid / waves) * 64 / waves - (chunks - 1) * 2;
             if (score > best_score) {
                 best_score = score;
                 best = SmallMPlan{split, (int)kc, (int)smem, occ};
             }
-            if (waves == 1) break;  // more chunks only shrink the chunk further
         }
     }
+    if (best1.split != 0) best = best1;
     if (best.split == 0) {
         // Nothing fit: the smallest chunk that is still whole ring stages and whole groups.
         const int kc = std::min(K / kKBlock, std::max(kBPS, bpg));
