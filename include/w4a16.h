@@ -100,6 +100,10 @@ size_t w4a16_gemm_workspace_bytes(int M, int N, int K, int group, int split_k);
 /*
  * Which path and split factor w4a16_gemm would use. split_k as in w4a16_gemm.
  * path / split_out are host pointers (either may be NULL).
+ * Path choice: M above the small-M limit (w4a16_set_tuning, default 64) takes
+ * the tensor-core path; so does M >= 40 when that path's grid (N/128 tiles, or
+ * N/64 for SwiGLU, times the token tiles) covers at least two thirds of the
+ * SMs, unless split_k > 0 forces the small-M path's K split.
  */
 w4a16_status w4a16_gemm_plan(int M, int N, int K, int group, int split_k,
                              int *path, int *split_out);
@@ -112,7 +116,8 @@ w4a16_status w4a16_gemm_plan(int M, int N, int K, int group, int split_k,
  *   zp       device uint8 [N][ceil(G/2)] packed zero points, or NULL (zero point 8)
  *   Y        device fp16 [M][N], written (no read-modify-write)
  *   split_k  0 = automatic; 1..8 forces the small-M path's K split (a cluster
- *            of that many CTAs per 128-row tile); ignored on the tensor-core path
+ *            of that many CTAs per 128-row tile) for M up to the small-M limit;
+ *            ignored on the tensor-core path
  *   ws, ws_bytes  caller scratch of at least w4a16_gemm_workspace_bytes(); may be
  *            NULL when that is 0
  * Small M (<= the small-M limit, 64 by default) runs the register-fed stream

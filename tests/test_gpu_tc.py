@@ -57,6 +57,17 @@ def test_mlp_large_m_sampled_rows(gpu_lib, M):
     check(run(gpu_lib, c, rows), ref, f"tc mlp M={M}")
 
 
+def test_path_choice(gpu_lib):
+    small, tc = gpu_lib.W4A16_PATH_SMALL_M, gpu_lib.W4A16_PATH_TCGEN05
+    assert gpu_lib.w4a16_gemm_plan(8, 13824, 5120, 128)[0] == small
+    assert gpu_lib.w4a16_gemm_plan(32, 13824, 5120, 128)[0] == small
+    # From 40 tokens on, a grid of 108 tiles makes the tensor-core kernel faster ...
+    assert gpu_lib.w4a16_gemm_plan(48, 13824, 5120, 128)[0] == tc
+    # ... but not one of 32 tiles, and a forced K split keeps the small-M path.
+    assert gpu_lib.w4a16_gemm_plan(48, 4096, 4096, 128)[0] == small
+    assert gpu_lib.w4a16_gemm_plan(48, 13824, 5120, 128, split_k=2) == (small, 2)
+
+
 @pytest.mark.parametrize("M", [1, 8, 33, 100, 300])
 @pytest.mark.parametrize("group", [16, 32, 64, 128])
 @pytest.mark.parametrize("sdt", [np.float16, np.float32])

@@ -70,11 +70,26 @@ struct Plan {
     int kc;
 };
 
+// The tensor-core kernel costs nearly the same for any M up to its token tile,
+// so from a few dozen tokens on it beats the stream kernel once its grid fills
+// most SMs. Measured on GB300 (us per call, stream kernel vs tensor-core
+// kernel): K=5120 N=13824 (108 tiles) M=32 37.5 vs 38.2, M=40 49.3 vs 38.5,
+// M=64 56.2 vs 38.6; K=N=4096 (32 tiles) M=64 15.8 vs 31.6.
+constexpr int kTcMinM = 40;
+bool tc_preferred(int M, int N, bool swiglu) {
+    if (M < kTcMinM) return false;
+    const int cols = swiglu ? 64 : kTileRows;  // output columns per tensor-core CTA
+    const int T = tc_tile_tokens(M, swiglu);
+    const long long ctas = (long long)((N + cols - 1) / cols) * ((M + T - 1) / T);
+    return 3 * ctas >= 2LL * sm_count();
+}
+
 w4a16_status make_plan(int M, int N, int K, int group, int split_k, bool swiglu, Plan *out) {
     if (split_k < 0 || split_k > 8) return W4A16_ERR_INVALID_ARG;
     Plan p{};
     const int smax = g_smallm_max;
-    if (M <= smax) {
+    // A forced K split exists only on the small-M path, so it keeps that path.
+    if (M <= smax && (split_k > 0 || !tc_preferred(M, N, swiglu))) {
         p.path = W4A16_PATH_SMALL_M;
         if (split_k > K / (group > kKBlock ? group : kKBlock)) return W4A16_ERR_UNSUPPORTED;
         const SmallMPlan sp = smallm_plan(M, N, K, group, swiglu, split_k, sm_count());
