@@ -61,7 +61,11 @@ struct Shape {
     static constexpr int CW = 8 / SUBT;             // consumer warps
     static constexpr int THREADS = CW * 32 + 32;    // + one producer warp
     static constexpr int STAGES = kStages;
-    static constexpr int MINB = SUBT == 2 ? 4 : (MT * NS <= 4 ? 2 : 1);
+    // CTAs per SM the register budget is sized for: fewer when the accumulators
+    // grow, so that they stay in registers (measured at K=5120 N=13824: M=9
+    // 16.4 vs 19.5 us, M=16 18.2 vs 20.3, M=32 32.6 vs 37.3 against the budget
+    // of one token tile, which spilled).
+    static constexpr int MINB = MT * NS == 1 ? 4 : (MT * NS == 2 ? 3 : 1);
 };
 
 // Compile-time loop: f(std::integral_constant<int, I>) for I in [B, E). Register
