@@ -104,6 +104,17 @@ def test_ragged_shapes(gpu_lib, M, N, K, group):
     check(run_gemm(gpu_lib, c), oracle.gemm(c.A, c.bq, c.scales, c.zp, group), f"ragged {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K,group", [(8, 8192, 28672, 128), (8, 28672, 8192, 64), (1, 8192, 28672, 16),
+                                         (300, 8192, 28672, 128), (48, 28672, 8192, 128)])
+def test_large_shapes_sampled_rows(gpu_lib, M, N, K, group):
+    # 70B-class projections (long K for the down projection): every column of a
+    # few token rows against the oracle.
+    c = make_case(M, N, K, group, seed=M + K)
+    rows = sorted({0, M // 2, M - 1})
+    Y = run_gemm(gpu_lib, c)[rows]
+    check(Y, oracle.gemm(c.A, c.bq, c.scales, c.zp, group, rows=rows), f"large {M}x{N}x{K} g={group}")
+
+
 def test_split_results_differ_only_by_rounding(gpu_lib):
     c = make_case(4, 1024, 2048, 128, seed=22)
     Ys = [run_gemm(gpu_lib, c, split_k=s).float() for s in (1, 2, 8)]
