@@ -75,9 +75,13 @@ struct Plan {
 // most SMs. Measured on GB300 (us per call, stream kernel vs tensor-core
 // kernel): K=5120 N=13824 (108 tiles) M=32 37.5 vs 38.2, M=40 49.3 vs 38.5,
 // M=64 56.2 vs 38.6; K=N=4096 (32 tiles) M=64 15.8 vs 31.6.
+// Fused SwiGLU switches at 33 tokens, where the small-M kernel would need four
+// 8-token tiles for two weight sets (K=5120 N=13824, us per call: M=24 48.9 vs
+// 75.3, M=33 126.9 vs 76.1).
 constexpr int kTcMinM = 40;
+constexpr int kTcMinMSwiglu = 33;
 bool tc_preferred(int M, int N, bool swiglu) {
-    if (M < kTcMinM) return false;
+    if (M < (swiglu ? kTcMinMSwiglu : kTcMinM)) return false;
     const int cols = swiglu ? 64 : kTileRows;  // output columns per tensor-core CTA
     const int T = tc_tile_tokens(M, swiglu);
     const long long ctas = (long long)((N + cols - 1) / cols) * ((M + T - 1) / T);
