@@ -47,7 +47,8 @@ namespace {
 
 constexpr int kPartStride = kTileRows + 4;          // floats per partial row (bank spread)
 constexpr int kBPS = 4;                             // k-blocks per ring stage
-constexpr int kStageSet = kTileRows * 32 * kBPS;    // 16 KB: one stage of one weight set
+constexpr int kBlkBytes = kTileRows * 32;           // 4 KB: one block slot of a stage
+constexpr int kStageSet = kBlkBytes * kBPS;         // 16 KB: one stage of one weight set
 
 // Ring stages of kStageSet bytes per weight set: 32 / 64 KB in flight per CTA.
 constexpr int kStages = 2;
@@ -240,9 +241,17 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                 ptx::mbar_arrive_expect_tx(&full[s], NS * bytes);
                 const size_t off = chunk_offset(n0, p.N, p.K, b0);
 #pragma unroll
-                for (int w = 0; w < NS; ++w)
-                    ptx::bulk_g2s_hint(smem + (size_t)(s * NS + w) * kStageSet, p.w[w].q_rep + off, bytes, &full[s],
-                                       stream_policy);
+                for (int w = 0; w < NS; ++w) {
+                    unsigned char *dst = smem + (size_t)(s * NS + w) * kStageSet;
+                    if (R == kTileRows) {  // full tile: the stage's blocks are one contiguous span
+                        ptx::bulk_g2s_hint(dst, p.w[w].q_rep + off, bytes, &full[s], stream_policy);
+                    } else {               // ragged last tile: one copy per 4 KB block slot
+                        const int nb = min(kBPS, b_end - b0);
+                        for (int i = 0; i < nb; ++i)
+                            ptx::bulk_g2s_hint(dst + i * kBlkBytes, p.w[w].q_rep + off + (size_t)i * blk_bytes,
+                                               blk_bytes, &full[s], stream_policy);
+                    }
+                }
             }
             if (!a_issued && !*abort_flag) start_activations();
             if (*abort_flag) {
@@ -367,79 +376,95 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                 const uint32_t ph = (uint32_t)(st / STAGES) & 1u;
                 if (!aborted && !ptx::mbar_wait(&full[s], ph, abort_flag, p.err)) aborted = true;
                 if (aborted) continue;
-                const unsigned char *ring = smem + (size_t)s * NS * kStageSet;
                 const int bs = b_begin + st * kBPS;  // first k-block of the stage
-                static_for<0, kBPS>([&](auto ic) {
-                    constexpr int i = decltype(ic)::value;
-                    const int b = bs + i;
-                    if (b >= c1) return;
-                    uint4 wv[NS][SUBT];
-                    static_for<0, NS>([&](auto wc) {
-                        constexpr int w = decltype(wc)::value;
-                        static_for<0, SUBT>([&](auto uc) {
-                            constexpr int u = decltype(uc)::value;
-                            wv[w][u] = *reinterpret_cast<const uint4 *>(ring + w * kStageSet + i * blk_bytes +
-                                                                       (warp * SUBT + u) * kSubBytes + slot * 16);
-                        });
-                    });
-                    const __half *ablk = sA + (b - c0) * kKBlock + 4 * t;
-                    static_for<0, 4>([&](auto jc) {
-                        constexpr int j = decltype(jc)::value;
-                        constexpr int step = i * 4 + j;  // k16 step within the stage
-                        // Activation fragment of each token tile: k = 16j + 4t .. +3.
-                        uint32_t bfr[MT][2];
-#pragma unroll
-                        for (int mt = 0; mt < MT; ++mt) {
-                            const uint2 v = *reinterpret_cast<const uint2 *>(ablk + arow[mt] + 16 * j);
-                            bfr[mt][0] = v.x;
-                            bfr[mt][1] = v.y;
-                        }
+                // Per-stage bases: every offset below them is a compile-time constant
+                // (weights sit in fixed 4 KB block slots, stages start on a group).
+                const unsigned char *wbase =
+                    smem + (size_t)s * NS * kStageSet + (warp * SUBT) * kSubBytes + slot * 16;
+                const __half *abase = sA + (bs - c0) * kKBlock + 4 * t;
+                const float2 *mbase = meta0 + ((bs - c0) * kKBlock) / GROUP;
+                auto run_stage = [&](auto nbc) {
+                    constexpr int NB = decltype(nbc)::value;
+                    static_for<0, NB>([&](auto ic) {
+                        constexpr int i = decltype(ic)::value;
+                        uint4 wv[NS][SUBT];
                         static_for<0, NS>([&](auto wc) {
                             constexpr int w = decltype(wc)::value;
                             static_for<0, SUBT>([&](auto uc) {
                                 constexpr int u = decltype(uc)::value;
-                                const uint32_t word = j == 0 ? wv[w][u].x : j == 1 ? wv[w][u].y
-                                                    : j == 2 ? wv[w][u].z : wv[w][u].w;
-                                const uint32_t w8 = word >> 8;
-                                uint32_t a[4];
-                                a[0] = lop_or<0x000F000Fu>(word);  // row g,   k 4t+0/1: 1024 + q
-                                a[1] = lop_or<0x00F000F0u>(word);  // row g+8, k 4t+0/1: 1024 + 16 q
-                                a[2] = lop_or<0x000F000Fu>(w8);    // row g,   k 4t+2/3
-                                a[3] = lop_or<0x00F000F0u>(w8);    // row g+8, k 4t+2/3
-#pragma unroll
-                                for (int mt = 0; mt < MT; ++mt) {
-                                    if constexpr (step % SPG == 0) {
-                                        const float z4[4] = {0.f, 0.f, 0.f, 0.f};
-                                        mma_16816(accg[w][u][mt], a, bfr[mt][0], bfr[mt][1], z4);
-                                    } else {
-                                        mma_16816(accg[w][u][mt], a, bfr[mt][0], bfr[mt][1], accg[w][u][mt]);
-                                    }
-                                }
+                                wv[w][u] = *reinterpret_cast<const uint4 *>(wbase + w * kStageSet + i * kBlkBytes +
+                                                                           u * kSubBytes);
                             });
                         });
-                        if constexpr (step % SPG == SPG - 1) {
-                            // Group complete: acc += (s / f) * acc_g.
-                            const int gi = (b * kKBlock + 16 * j) / GROUP - grp0;
+                        static_for<0, 4>([&](auto jc) {
+                            constexpr int j = decltype(jc)::value;
+                            constexpr int step = i * 4 + j;  // k16 step within the stage
+                            // Activation fragment of each token tile: k = 16j + 4t .. +3.
+                            uint32_t bfr[MT][2];
+#pragma unroll
+                            for (int mt = 0; mt < MT; ++mt) {
+                                const uint2 v =
+                                    *reinterpret_cast<const uint2 *>(abase + arow[mt] + i * kKBlock + 16 * j);
+                                bfr[mt][0] = v.x;
+                                bfr[mt][1] = v.y;
+                            }
                             static_for<0, NS>([&](auto wc) {
                                 constexpr int w = decltype(wc)::value;
                                 static_for<0, SUBT>([&](auto uc) {
                                     constexpr int u = decltype(uc)::value;
-                                    const float s0 = meta0[w * meta_set + mrow[u][0] + gi].x;
-                                    const float s1 = meta0[w * meta_set + mrow[u][1] + gi].x;
+                                    const uint32_t word = j == 0 ? wv[w][u].x : j == 1 ? wv[w][u].y
+                                                        : j == 2 ? wv[w][u].z : wv[w][u].w;
+                                    const uint32_t w8 = word >> 8;
+                                    uint32_t a[4];
+                                    a[0] = lop_or<0x000F000Fu>(word);  // row g,   k 4t+0/1: 1024 + q
+                                    a[1] = lop_or<0x00F000F0u>(word);  // row g+8, k 4t+0/1: 1024 + 16 q
+                                    a[2] = lop_or<0x000F000Fu>(w8);    // row g,   k 4t+2/3
+                                    a[3] = lop_or<0x00F000F0u>(w8);    // row g+8, k 4t+2/3
 #pragma unroll
                                     for (int mt = 0; mt < MT; ++mt) {
-                                        float *ac = acc[w][u][mt];
-                                        const float *ag = accg[w][u][mt];
-                                        ac[0] = fmaf(s0, ag[0], ac[0]);
-                                        ac[1] = fmaf(s0, ag[1], ac[1]);
-                                        ac[2] = fmaf(s1, ag[2], ac[2]);
-                                        ac[3] = fmaf(s1, ag[3], ac[3]);
+                                        if constexpr (step % SPG == 0) {
+                                            const float z4[4] = {0.f, 0.f, 0.f, 0.f};
+                                            mma_16816(accg[w][u][mt], a, bfr[mt][0], bfr[mt][1], z4);
+                                        } else {
+                                            mma_16816(accg[w][u][mt], a, bfr[mt][0], bfr[mt][1], accg[w][u][mt]);
+                                        }
                                     }
                                 });
                             });
-                        }
+                            if constexpr (step % SPG == SPG - 1) {
+                                // Group complete: acc += (s / f) * acc_g.
+                                constexpr int gs = (i * kKBlock + 16 * j) / GROUP;  // group within the stage
+                                static_for<0, NS>([&](auto wc) {
+                                    constexpr int w = decltype(wc)::value;
+                                    static_for<0, SUBT>([&](auto uc) {
+                                        constexpr int u = decltype(uc)::value;
+                                        const float s0 = mbase[w * meta_set + mrow[u][0] + gs].x;
+                                        const float s1 = mbase[w * meta_set + mrow[u][1] + gs].x;
+#pragma unroll
+                                        for (int mt = 0; mt < MT; ++mt) {
+                                            float *ac = acc[w][u][mt];
+                                            const float *ag = accg[w][u][mt];
+                                            ac[0] = fmaf(s0, ag[0], ac[0]);
+                                            ac[1] = fmaf(s0, ag[1], ac[1]);
+                                            ac[2] = fmaf(s1, ag[2], ac[2]);
+                                            ac[3] = fmaf(s1, ag[3], ac[3]);
+                                        }
+                                    });
+                                });
+                            }
+                        });
                     });
-                });
+                };
+                const int nb = min(kBPS, c1 - bs);  // blocks of this stage (whole groups)
+                if (nb == kBPS) {
+                    run_stage(std::integral_constant<int, kBPS>{});
+                } else if constexpr (BPG == 1) {
+                    if (nb == 1) run_stage(std::integral_constant<int, 1>{});
+                    else if (nb == 2) run_stage(std::integral_constant<int, 2>{});
+                    else run_stage(std::integral_constant<int, 3>{});
+                } else {
+                    run_stage(std::integral_constant<int, 2>{});  // 128-wide groups: two blocks
+                }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&empty[s]);
             }
