@@ -36,7 +36,7 @@ METRIC = "W4A16 GEMM us per call (HBM roofline at M<=8)"
 # hash of the kernel source it was taken on (reported as null once the source
 # changes). Filled from profiles/ summaries.
 NCU_TRAFFIC = {
-    "ceda135fc3ba1f9b": 36925184,  # dram read + write, profiles/smallm_kernel_mlp_m8_K5120_N13824_g128.md
+    "4bcfe4cf1fd560c8": 36925184,  # dram read + write, profiles/smallm_kernel_mlp_m8_K5120_N13824_g128.md
 }
 
 

@@ -182,20 +182,42 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
     constexpr int PREB = RPT == 1 ? 2 : 1;  // prefetched batches of 8 groups
     float pre_s[RPT][PREB][8];
     uint32_t pre_z[RPT][PREB][8];
-    auto load_meta_batch = [&](int row_set, int grp_first, int count, float (&sv)[8], uint32_t (&zb)[8]) {
+    // One batch = the 8 groups gbase .. gbase+7 of one row (gbase a multiple of 8);
+    // groups outside [lo, hi) are not needed. fp16 scales in rows that start 16-byte
+    // aligned (G % 8 == 0) come from one 16-byte load, their zero points from one
+    // 4-byte load; other formats load each group.
+    auto load_meta_batch = [&](int row_set, int gbase, int lo, int hi, float (&sv)[8], uint32_t (&zb)[8]) {
         const int w = row_set / kTileRows, row = row_set % kTileRows;
         const int n = n0 + row;
         const uint8_t *zrow = p.w[w].zp ? p.w[w].zp + (size_t)n * zpstride : nullptr;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int grp = grp_first + u;
             sv[u] = 0.f;
             zb[u] = 0x88u;
-            if (u < count && row < R) {
-                const size_t si = (size_t)n * p.G + grp;
-                sv[u] = p.scale_f32 ? __ldg(reinterpret_cast<const float *>(p.w[w].scales) + si)
-                                    : __half2float(__ldg(reinterpret_cast<const __half *>(p.w[w].scales) + si));
-                if (zrow) zb[u] = __ldg(zrow + (grp >> 1));
+        }
+        // No load for a window that holds none of the needed groups (it may lie
+        // past the end of the row); a window that does ends inside its row.
+        if (row >= R || gbase >= hi || gbase + 8 <= lo) return;
+        if (!p.scale_f32 && (p.G & 7) == 0) {
+            const uint4 x = __ldg(reinterpret_cast<const uint4 *>(
+                reinterpret_cast<const unsigned short *>(p.w[w].scales) + (size_t)n * p.G + gbase));
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+            const uint32_t zw = zrow ? __ldg(reinterpret_cast<const unsigned int *>(zrow + gbase / 2)) : 0x88888888u;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                sv[u] = __half2float(__ushort_as_half((unsigned short)(xs[u >> 1] >> (16 * (u & 1)))));
+                zb[u] = (zw >> (8 * (u >> 1))) & 0xFFu;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int grp = gbase + u;
+                if (grp >= lo && grp < hi) {
+                    const size_t si = (size_t)n * p.G + grp;
+                    sv[u] = p.scale_f32 ? __ldg(reinterpret_cast<const float *>(p.w[w].scales) + si)
+                                        : __half2float(__ldg(reinterpret_cast<const __half *>(p.w[w].scales) + si));
+                    if (zrow) zb[u] = __ldg(zrow + (grp >> 1));
+                }
             }
         }
     };
@@ -208,7 +230,8 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
             if (rs < NS * kTileRows) {
 #pragma unroll
                 for (int bt = 0; bt < PREB; ++bt)
-                    load_meta_batch(rs, grp_first0 + 8 * bt, min(8, ng_first0 - 8 * bt), pre_s[r][bt], pre_z[r][bt]);
+                    load_meta_batch(rs, (grp_first0 & ~7) + 8 * bt, grp_first0, grp_first0 + ng_first0, pre_s[r][bt],
+                                    pre_z[r][bt]);
             }
         }
     }
@@ -317,26 +340,29 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                 if (row >= R) continue;
                 float2 *meta = reinterpret_cast<float2 *>(smem + plan.meta_off + w * plan.meta_set_bytes) +
                                (size_t)row * plan.ng;
-                const float f = ((row >> 3) & 1) ? 16.f : 1.f;
-                for (int gb = 0; gb < ng; gb += 8) {
+                const bool hi_row = (row >> 3) & 1;
+                const float f = hi_row ? 16.f : 1.f, inv_f = hi_row ? 0.0625f : 1.f;
+                const int gbase0 = grp0 & ~7;  // batches start on 8-group boundaries
+                for (int gb = gbase0; gb < grp0 + ng; gb += 8) {
+                    const int bt = (gb - gbase0) >> 3;
                     float sv[8];
                     uint32_t zb[8];
-                    if (c0 == b_begin && gb < 8 * PREB) {
+                    if (c0 == b_begin && bt < PREB) {
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
-                            sv[u] = gb == 0 ? pre_s[r][0][u] : pre_s[r][PREB - 1][u];
-                            zb[u] = gb == 0 ? pre_z[r][0][u] : pre_z[r][PREB - 1][u];
+                            sv[u] = bt == 0 ? pre_s[r][0][u] : pre_s[r][PREB - 1][u];
+                            zb[u] = bt == 0 ? pre_z[r][0][u] : pre_z[r][PREB - 1][u];
                         }
                     } else {
-                        load_meta_batch(rs, grp0 + gb, min(8, ng - gb), sv, zb);
+                        load_meta_batch(rs, gb, grp0, grp0 + ng, sv, zb);
                     }
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
-                        if (gb + u < ng) {
-                            const int grp = grp0 + gb + u;
+                        const int grp = gb + u, gi = grp - grp0;
+                        if (gi >= 0 && gi < ng) {
                             const float zv = (float)((grp & 1) ? (zb[u] >> 4) : (zb[u] & 0xFu));
-                            const float sf = sv[u] / f;
-                            meta[gb + u] = make_float2(sf, sf * (1024.f + f * zv));
+                            const float sf = sv[u] * inv_f;  // exact: f is a power of two
+                            meta[gi] = make_float2(sf, sf * (1024.f + f * zv));
                         }
                     }
                 }
