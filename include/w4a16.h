@@ -121,12 +121,12 @@ w4a16_status w4a16_gemm_plan(int M, int N, int K, int group, int split_k,
  *            ignored on the tensor-core path
  *   ws, ws_bytes  caller scratch of at least w4a16_gemm_workspace_bytes(); may be
  *            NULL when that is 0
- * Small M (<= the small-M limit, 64 by default) runs the register-fed stream
- * kernel: 128-bit coalesced weight loads, dequantisation in registers, mma.sync
- * m16n8k16 with fp32 accumulation and the group scale applied after each group's
- * partial sum (the pull request's "per-group scale AFTER the tensor-core
- * accumulate"), K split across a cluster and reduced in a fixed order. Larger M
- * runs the tcgen05 kernel: TMA-staged activations, int4 tiles dequantised to fp16
+ * Small M (see w4a16_gemm_plan for the choice) runs the stream kernel: weights
+ * streamed by bulk copies through a shared-memory ring, dequantisation in
+ * registers, mma.sync m16n8k16 with fp32 accumulation and the group scale applied
+ * after each group's partial sum (the pull request's "per-group scale AFTER the
+ * tensor-core accumulate"), K split across a cluster and reduced in a fixed order.
+ * Larger M runs the tcgen05 kernel: TMA-staged activations, int4 tiles dequantised to fp16
  * ((q - zp) * scale rounded once; fp32 scales are rounded to fp16 first) into
  * tensor memory, fp32 accumulation in tensor memory.
  */
@@ -186,8 +186,8 @@ w4a16_status w4a16_gemm_swiglu_unfused_static(const uint16_t *A,
 
 /*
  * Tuning knobs (process-wide, not thread-safe; for tests and benchmarks).
- *   smallm_max  largest M routed to the small-M path (0 = default 64, max 64;
- *               -1 routes every M to the tensor-core path)
+ *   smallm_max  largest M that may take the small-M path (0 = default 64, max 64;
+ *               -1 routes every M to the tensor-core path); see w4a16_gemm_plan
  */
 w4a16_status w4a16_set_tuning(int smallm_max);
 
