@@ -36,7 +36,7 @@ METRIC = "W4A16 GEMM us per call (HBM roofline at M<=8)"
 # hash of the kernel source it was taken on (reported as null once the source
 # changes). Filled from profiles/ summaries.
 NCU_TRAFFIC = {
-    "4bcfe4cf1fd560c8": 36925184,  # dram read + write, profiles/smallm_kernel_mlp_m8_K5120_N13824_g128.md
+    "1e9197a8b67e1772": 36925184,  # dram read + write, profiles/smallm_kernel_mlp_m8_K5120_N13824_g128.md
 }
 
 
@@ -56,10 +56,16 @@ def load_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the small-M kernel's code (comments and blank space removed), so
+    that recorded ncu counters stay attached to the code they were taken on."""
+    import re
     h = hashlib.sha256()
     for f in ("gemm_smallm.cu", "ptx.cuh", "w4a16_internal.h"):
-        with open(os.path.join(ROOT, "weight_only_int4_repack_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "weight_only_int4_repack_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

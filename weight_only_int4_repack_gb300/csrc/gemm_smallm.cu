@@ -9,10 +9,12 @@
 //   * one CTA = one 128-row tile x one K range. In the repacked layout that
 //     range is one contiguous span, so a producer warp streams it through a
 //     shared-memory ring with 16 KB cp.async.bulk copies (four 64-k blocks per
-//     stage), starting at kernel entry: the weight stream is already in flight
-//     while the CTA stages activations and metadata. (Measured on GB300: 1-D
-//     bulk copies reach HBM speed with 8-16 KB pieces; with 4 KB pieces a CTA
-//     completed only about one copy per half microsecond.)
+//     stage). The stream starts once the CTA's scales and zero points have
+//     landed: they gate every group's flush, and issuing weights earlier
+//     measured slower. (Measured on GB300: 1-D bulk copies reach HBM speed with
+//     8-16 KB pieces; with 4 KB pieces a CTA completed only about one copy per
+//     half microsecond.) The K split is chosen per shape so that the busiest SM
+//     streams as few weight bytes as possible;
 //   * consumer warps own one or two 16-row sub-tiles; a lane reads one 16-byte
 //     slot per sub-tile and block (a conflict-free 128-bit shared load) whose
 //     four words are mma.sync.m16n8k16 A fragments for four k16 steps; the
