@@ -32,11 +32,11 @@ M, N, K, GROUP, SEED = 8, 13824, 5120, 128, 2
 WORKLOAD = f"mlp-projection W4A16 GEMM M={M} K={K} N={N} group={GROUP} asym-zp fp16-scales"
 METRIC = "W4A16 GEMM us per call (HBM roofline at M<=8)"
 
-# DRAM traffic per launch of the small-M kernel from an ncu capture, keyed by a
-# hash of the kernel source it was taken on (reported as null once the source
-# changes). Filled from profiles/ summaries.
+# DRAM traffic per launch of the small-M kernel from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by a hash of the kernel
+# source it was taken on; reported as null once the source changes.
 NCU_TRAFFIC = {
-    "1e9197a8b67e1772": 36925184,  # dram read + write, profiles/smallm_kernel_mlp_m8_K5120_N13824_g128.md
+    "1e9197a8b67e1772": 36925184,
 }
 
 

@@ -208,6 +208,21 @@ w4a16_status w4a16_set_tuning(int smallm_max);
 w4a16_status w4a16_set_launch_overlap(int enable);
 
 /*
+ * Limit of every bounded device-side wait (process-wide, not thread-safe; for
+ * tests of the failure path). Each wait for an mbarrier phase (a copy landing,
+ * a pipeline slot freeing up, the accumulator completing) gives up once it has
+ * waited limit_ns or longer: the kernel then records W4A16_ERR_TIMEOUT in the
+ * device error word (see w4a16_device_error), stops issuing work, waits for the
+ * copies and tensor-core operations it already issued (with a fixed limit of
+ * 0.2 s), releases its tensor memory and returns; its output is undefined.
+ * Default 2000000000 (2 s). 0 gives up at the first poll that finds a phase
+ * incomplete, which makes any call whose copies are still in flight fail; this
+ * exists so that tests can run the expiry path without a stuck barrier.
+ * Always returns W4A16_OK.
+ */
+w4a16_status w4a16_set_wait_limit_ns(unsigned long long limit_ns);
+
+/*
  * Read and clear the device-side error word that bounded waits set when they
  * expire (W4A16_ERR_TIMEOUT) on the device current for the calling thread.
  * Synchronises `stream`. Returns W4A16_OK when no kernel reported an error.

@@ -156,6 +156,48 @@ def gemm_swiglu(A, gate, up, group: int, rows=None, cols=None,
     return Y
 
 
+def rmsnorm(A, gamma, eps: float) -> np.ndarray:
+    """RMS normalisation of each activation row, float64 (the RMS-norm prologue
+    of the same pull request, "Update -- fused RMS-norm epilogue + e2e PASS" and
+    "Update -- P1 COMPLETE": the normalised activation is staged, then the GEMM
+    runs on it). Reading of the pages, which give no formula: the ONNX
+    SimplifiedLayerNormalization that the prologue replaces,
+
+        out[m, k] = A[m, k] / sqrt(mean_k(A[m, k]^2) + eps) * gamma[k].
+
+    Plain float64 arithmetic on the widened inputs; no rounding of the result."""
+    A64 = _f64(A)
+    g64 = _f64(gamma).reshape(-1)
+    if A64.ndim != 2 or g64.size != A64.shape[1]:
+        raise ValueError("A must be [M, K] and gamma [K]")
+    M, K = A64.shape
+    out = np.empty_like(A64)
+    for m in range(M):
+        row = A64[m]
+        r = 1.0 / np.sqrt(float(np.dot(row, row)) / K + float(eps))
+        out[m] = row * r * g64
+    return out
+
+
+def _rows_of(A, rows):
+    A = np.asarray(A)
+    return A if rows is None else A[np.asarray(rows)]
+
+
+def gemm_rmsnorm(A, gamma, eps: float, bq, scales, zp, group: int, rows=None, cols=None,
+                 nthreads: Optional[int] = None) -> np.ndarray:
+    """Y = rmsnorm(A) . dequant(Bq)^T in float64 (optionally only some rows of A)."""
+    return gemm(rmsnorm(_rows_of(A, rows), gamma, eps), bq, scales, zp, group, cols=cols,
+                nthreads=nthreads)
+
+
+def gemm_swiglu_rmsnorm(A, gamma, eps: float, gate, up, group: int, rows=None, cols=None,
+                        nthreads: Optional[int] = None) -> np.ndarray:
+    """Y = silu(rmsnorm(A) . Wg^T) * (rmsnorm(A) . Wu^T) in float64."""
+    return gemm_swiglu(rmsnorm(_rows_of(A, rows), gamma, eps), gate, up, group, cols=cols,
+                       nthreads=nthreads)
+
+
 def repack(bq) -> np.ndarray:
     return repack_layout.repack(_u8(bq))
 

@@ -48,7 +48,7 @@ def run(w4, c, rows=None):
     return y if rows is None else y[rows]
 
 
-@pytest.mark.parametrize("M", [65, 128, 200, 256, 1024])
+@pytest.mark.parametrize("M", [65, 128, 200, 256, 1024, 4096])
 def test_mlp_large_m_sampled_rows(gpu_lib, M):
     assert gpu_lib.w4a16_gemm_plan(M, 13824, 5120, 128)[0] == gpu_lib.W4A16_PATH_TCGEN05
     c = make_case(M, 13824, 5120, 128, seed=2)
@@ -97,7 +97,7 @@ def test_small_and_tc_paths_agree(gpu_lib):
     check(y_tc, ref, "tc path")
 
 
-@pytest.mark.parametrize("M", [256, 1024])
+@pytest.mark.parametrize("M", [256, 1024, 4096, 8192])
 @pytest.mark.parametrize("fused", [True, False])
 def test_swiglu_large_m(gpu_lib, M, fused):
     gc, uc = make_swiglu_case(M, 13824, 5120, 128, seed=4)

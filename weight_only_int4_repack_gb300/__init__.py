@@ -43,6 +43,7 @@ EXPORTS = (
     "w4a16_gemm_workspace_bytes", "w4a16_gemm_plan", "w4a16_gemm",
     "w4a16_swiglu_workspace_bytes", "w4a16_gemm_swiglu", "w4a16_set_tuning", "w4a16_set_launch_overlap",
     "w4a16_device_error", "w4a16_swiglu_static_scratch_bytes", "w4a16_gemm_swiglu_unfused_static",
+    "w4a16_set_wait_limit_ns",
 )
 
 _vp, _ci, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -60,6 +61,7 @@ _sig = {
     "w4a16_set_tuning": (_ci, [_ci]),
     "w4a16_set_launch_overlap": (_ci, [_ci]),
     "w4a16_device_error": (_ci, [_vp]),
+    "w4a16_set_wait_limit_ns": (_ci, [ctypes.c_ulonglong]),
     "w4a16_swiglu_static_scratch_bytes": (_sz, []),
     "w4a16_gemm_swiglu_unfused_static": (_ci, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _vp,
                                                _ci, _ci, _ci, _ci, _vp]),
@@ -208,6 +210,14 @@ def w4a16_set_launch_overlap(enable: bool) -> None:
     """Let small-M GEMM calls start while the work before them finishes
     (weights must not be written by that work); see include/w4a16.h."""
     _check(lib.w4a16_set_launch_overlap(int(enable)), "w4a16_set_launch_overlap")
+
+
+WAIT_LIMIT_DEFAULT_NS = 2_000_000_000
+
+
+def w4a16_set_wait_limit_ns(limit_ns: int) -> None:
+    """Limit of every bounded device-side wait (tests of the failure path)."""
+    _check(lib.w4a16_set_wait_limit_ns(int(limit_ns)), "w4a16_set_wait_limit_ns")
 
 
 def w4a16_device_error(stream=None) -> int:

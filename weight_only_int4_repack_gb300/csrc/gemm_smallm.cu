@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                 const int s = st % STAGES;
                 const uint32_t ph = (uint32_t)(st / STAGES) & 1u;
                 if (st == pre && !a_issued) start_activations();
-                if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err)) break;
+                if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err, p.wait_ns)) break;
                 const int b0 = b_begin + st * kBPS;
                 const uint32_t bytes = blk_bytes * (uint32_t)min(kBPS, b_end - b0);
                 ptx::mbar_arrive_expect_tx(&full[s], NS * bytes);
@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                 }
             }
             const int chunk_idx = (c0 - b_begin) / kc;
-            if (!aborted && !ptx::mbar_wait(abar, (uint32_t)chunk_idx & 1u, abort_flag, p.err)) aborted = true;
+            if (!aborted && !ptx::mbar_wait(abar, (uint32_t)chunk_idx & 1u, abort_flag, p.err, p.wait_ns)) aborted = true;
             // Group activation sums A_g[token] of this chunk (fp32 over the fp16
             // values), one (group, token) per thread with independent loads.
             {
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
             for (int st = st0; st < st1; ++st) {
                 const int s = st % STAGES;
                 const uint32_t ph = (uint32_t)(st / STAGES) & 1u;
-                if (!aborted && !ptx::mbar_wait(&full[s], ph, abort_flag, p.err)) aborted = true;
+                if (!aborted && !ptx::mbar_wait(&full[s], ph, abort_flag, p.err, p.wait_ns)) aborted = true;
                 if (aborted) continue;
                 const int bs = b_begin + st * kBPS;  // first k-block of the stage
                 // Per-stage bases: every offset below them is a compile-time constant
@@ -584,17 +584,7 @@ constexpr int kMaxDynSmem = 227 * 1024;
 // Raise the kernel's dynamic shared-memory limit once per device.
 template <int GROUP, int MT, bool SWIGLU>
 cudaError_t configure() {
-    static bool done[64] = {false};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && !done[dev]) {
-        e = cudaFuncSetAttribute(smallm_kernel<GROUP, MT, SWIGLU>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
-        if (e != cudaSuccess) return e;
-        done[dev] = true;
-    }
-    return cudaSuccess;
+    return ensure_max_dyn_smem(reinterpret_cast<const void *>(smallm_kernel<GROUP, MT, SWIGLU>), kMaxDynSmem);
 }
 
 // CTAs of a (1 x split) cluster launch that the device keeps resident at once.

@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (; kb < nkb; ++kb) {
                 const int s = kb % STAGES;
                 const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-                if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err)) break;
+                if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err, p.wait_ns)) break;
                 const uint32_t wbytes = (uint32_t)R * 32u;  // this CTA's rows of one weight set
                 ptx::mbar_arrive_expect_tx(&full[s], (uint32_t)L.b_stage + (SWIGLU ? 2u : 1u) * wbytes);
                 ptx::tma_load_2d(smem + (size_t)s * L.b_stage, &tmap_a, kb * kKBlock, m0, &full[s]);
@@ -283,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (; kb < nkb; ++kb) {
                 const int s = kb % STAGES, sa = kb % ASTAGES;
                 const uint32_t ph = (uint32_t)(kb / STAGES) & 1u, pa = (uint32_t)(kb / ASTAGES) & 1u;
-                if (!ptx::mbar_wait(&full[s], ph, abort_flag, p.err)) break;
-                if (!ptx::mbar_wait(&afull[sa], pa, abort_flag, p.err)) break;
+                if (!ptx::mbar_wait(&full[s], ph, abort_flag, p.err, p.wait_ns)) break;
+                if (!ptx::mbar_wait(&afull[sa], pa, abort_flag, p.err, p.wait_ns)) break;
                 tc_fence_after();
                 const uint32_t b_base = ptx::smem_u32(smem + (size_t)s * L.b_stage);
 #pragma unroll
@@ -330,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < nkb; ++kb) {
             const int s = kb % STAGES, sa = kb % ASTAGES;
             const uint32_t ph = (uint32_t)(kb / STAGES) & 1u, pa = (uint32_t)(kb / ASTAGES) & 1u;
-            if (!aborted && !ptx::mbar_wait(&full[s], ph, abort_flag, p.err)) aborted = true;
-            if (!aborted && !ptx::mbar_wait(&aempty[sa], pa ^ 1u, abort_flag, p.err)) aborted = true;
+            if (!aborted && !ptx::mbar_wait(&full[s], ph, abort_flag, p.err, p.wait_ns)) aborted = true;
+            if (!aborted && !ptx::mbar_wait(&aempty[sa], pa ^ 1u, abort_flag, p.err, p.wait_ns)) aborted = true;
             if (aborted) break;
             // Next block's metadata, loaded early (it is used one block later).
             uint32_t zzn[NS][kSPW], ssn[NS][kSPW];
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Epilogue: D[row r][token] -> Y[m0 + token][n]; the warps of a lane
         // quarter take alternate 16-column chunks.
-        const bool acc_ok = !aborted && ptx::mbar_wait(accfull, 0u, abort_flag, p.err);
+        const bool acc_ok = !aborted && ptx::mbar_wait(accfull, 0u, abort_flag, p.err, p.wait_ns);
         if constexpr (!SWIGLU) {
             if (acc_ok) {
                 tc_fence_after();
@@ -495,14 +495,8 @@ cudaError_t launch_tc_one(const TcParams &p, int T, cudaStream_t s) {
     // One CTA per SM: the kernel takes all 512 tensor-memory columns.
     const size_t smem = (L.total + 1024 > 120 * 1024) ? L.total + 1024 : 120 * 1024;
     auto kern = tc_kernel<GROUP, SWIGLU>;
-    static bool configured[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
+    cudaError_t e = ensure_max_dyn_smem(reinterpret_cast<const void *>(kern), 227 * 1024);
+    if (e != cudaSuccess) return e;
     const int cols = SWIGLU ? 64 : kTileRows;  // output columns per CTA
     dim3 grid((unsigned)((p.M + T - 1) / T), (unsigned)((p.N + cols - 1) / cols), 1);
     kern<<<grid, kThreads, smem, s>>>(map, p, T);

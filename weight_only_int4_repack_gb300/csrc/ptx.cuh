@@ -62,25 +62,29 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0;
 }
 
-// Wait for the phase with the given parity. Gives up after `limit_ns`
-// (default two seconds): records W4A16_ERR_TIMEOUT in *err, raises the CTA's
-// abort flag and returns false. Also returns false once another thread of the
-// CTA has raised the abort flag.
+// Default limit of a bounded wait: two seconds.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Wait for the phase with the given parity. Gives up once it has waited
+// `limit_ns` or longer (a limit of 0 gives up at the first poll that finds the
+// phase incomplete): records W4A16_ERR_TIMEOUT in *err, raises the CTA's abort
+// flag and returns false. Also returns false once another thread of the CTA has
+// raised the abort flag.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned int *err, uint64_t limit_ns = 2000000000ull) {
+                                          unsigned int *err, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
 #pragma unroll 1
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    for (uint32_t it = 0;; ++it) {
         if ((it & 63u) == 0) {  // the abort flag and the clock are checked now and then
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > limit_ns) {
+            if (globaltimer() - t0 >= limit_ns) {
                 if (err) atomicExch(err, (unsigned int)W4A16_ERR_TIMEOUT);
                 *abort_flag = 1;
                 return false;
             }
         }
+        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
     }
 }
 

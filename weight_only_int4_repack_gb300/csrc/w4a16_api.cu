@@ -4,6 +4,8 @@
 #include <climits>
 #include <cstring>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "w4a16_internal.h"
 
@@ -13,16 +15,22 @@ namespace {
 
 int g_smallm_max = kSmallMMaxM;
 int g_launch_overlap = 0;  // small-M launches as programmatic dependents
+unsigned long long g_wait_ns = 2000000000ull;  // limit of every bounded device-side wait
 
 __device__ unsigned int g_device_error;  // set by bounded waits that expire
 
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Per-device caches below are filled on first use under this lock, so that
+// concurrent first calls from several host threads are well defined.
+std::mutex g_cache_mu;
 
 // Device address of the error word on the current device (looked up once per device).
 unsigned int *device_error_ptr() {
     static unsigned int *cached[64] = {nullptr};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_cache_mu);
     if (!cached[dev]) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return nullptr;
@@ -31,10 +39,26 @@ unsigned int *device_error_ptr() {
     return cached[dev];
 }
 
-int sm_count() {
+}  // namespace
+
+cudaError_t w4a16::ensure_max_dyn_smem(const void *func, int bytes) {
+    static std::set<std::pair<const void *, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    if (done.count({func, dev})) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert({func, dev});
+    return e;
+}
+
+// Number of SMs of the current device (queried once per device).
+int w4a16::sm_count() {
     static int cached[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lock(g_cache_mu);
     if (!cached[dev]) {
         int n = 0;
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
@@ -43,6 +67,8 @@ int sm_count() {
     }
     return cached[dev];
 }
+
+namespace {
 
 w4a16_status check_shape(int M, int N, int K, int group) {
     if (M <= 0 || N <= 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
@@ -249,6 +275,7 @@ static w4a16_status gemm_impl(const uint16_t *A, const WeightSet *ws_sets, int n
         t.M = M; t.N = N; t.K = K; t.G = K / group;
         t.scale_f32 = sdt == W4A16_SCALE_F32;
         t.err = err;
+        t.wait_ns = g_wait_ns;
         return from_cuda(launch_tc(t, group, nsets == 2, stream));
     }
     SmallMParams p{};
@@ -262,6 +289,7 @@ static w4a16_status gemm_impl(const uint16_t *A, const WeightSet *ws_sets, int n
     p.kc_blocks = plan.kc;
     p.overlap = g_launch_overlap;
     p.err = err;
+    p.wait_ns = g_wait_ns;
     return from_cuda(launch_smallm(p, group, nsets == 2, stream));
 }
 
@@ -325,6 +353,11 @@ w4a16_status w4a16_set_tuning(int smallm_max) {
 w4a16_status w4a16_set_launch_overlap(int enable) {
     if (enable != 0 && enable != 1) return W4A16_ERR_INVALID_ARG;
     g_launch_overlap = enable;
+    return W4A16_OK;
+}
+
+w4a16_status w4a16_set_wait_limit_ns(unsigned long long limit_ns) {
+    g_wait_ns = limit_ns;
     return W4A16_OK;
 }
 

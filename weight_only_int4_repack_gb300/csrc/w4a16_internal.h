@@ -41,6 +41,7 @@ struct SmallMParams {
     int kc_blocks;          // k-blocks per staged activation chunk
     int overlap;            // launched as a programmatic dependent (weights read before the wait)
     unsigned int *err;      // device error word for bounded waits
+    unsigned long long wait_ns;  // limit of each bounded wait
 };
 
 struct TcParams {
@@ -50,7 +51,15 @@ struct TcParams {
     int M, N, K, G;
     int scale_f32;
     unsigned int *err;      // device error word for bounded waits
+    unsigned long long wait_ns;  // limit of each bounded wait
 };
+
+// Number of SMs of the current device (cached per device, thread-safe).
+int sm_count();
+
+// Raise `func`'s dynamic shared-memory limit to `bytes` once per device
+// (thread-safe; later calls for the same kernel and device do nothing).
+cudaError_t ensure_max_dyn_smem(const void *func, int bytes);
 
 // Host-side launchers (return cudaError_t of the launch).
 cudaError_t launch_repack(const uint8_t *q, uint8_t *q_rep, int N, int K, cudaStream_t s);
