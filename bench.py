@@ -339,8 +339,9 @@ def run_ours(args):
     }
 
     w4.w4a16_set_launch_overlap(False)
+    checks = []
     if rank == 0 and not args.no_extras:
-        out["extras"] = extras(args, w4, torch, device, stream, l2)
+        out["extras"] = extras(args, w4, torch, device, stream, l2, checks)
 
     if rank == 0 and not args.no_cpu_baseline:
         us_cpu, reps, _, Yref = oracle_time_per_call(case, budget_s=args.cpu_seconds)
@@ -351,6 +352,10 @@ def run_ours(args):
                                "kind": "oracle",
                                "sample": f"full M={M} call (all {N} columns), {reps} repetitions"}
         out["parity"] = {"max_abs_err": err, "tol": tol, "pass": err <= tol}
+        if checks:
+            ok, per_shape = check_parity(checks)
+            out["parity"]["extras_all_pass"] = ok
+            out["parity"]["extras"] = per_shape
     if rank == 0:
         print(json.dumps(out))
     if world > 1:
@@ -359,6 +364,12 @@ def run_ours(args):
 
 def time_calls(torch, stream, fn, n_calls, reps=1):
     """Median over `reps` of the mean device time per call (graph of n_calls calls)."""
+    return statistics.median(sample_calls(torch, stream, fn, n_calls, reps))
+
+
+def sample_calls(torch, stream, fn, n_calls, reps):
+    """`reps` samples of the mean device time per call (us), each one replay of a
+    CUDA graph of n_calls calls bracketed by CUDA events on `stream`."""
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         for i in range(3):
@@ -380,157 +391,268 @@ def time_calls(torch, stream, fn, n_calls, reps=1):
             stream.synchronize()
             out.append(e0.elapsed_time(e1) * 1e3 / n_calls)
     del g
-    return statistics.median(out)
+    return out
 
 
-def extras(args, w4, torch, device, stream, l2):
-    """Secondary measurements: M sweeps, decode shape, SwiGLU fused vs unfused, repack."""
-    from w4a16_inputs import make_case, make_swiglu_case
-    hbm_peak, _, _ = load_peaks()
+def spread(xs):
+    xs = sorted(xs)
+    q = lambda f: xs[min(len(xs) - 1, int(round(f * (len(xs) - 1))))]  # noqa: E731
+    return {"median": round(statistics.median(xs), 3), "p10": round(q(0.1), 3), "p90": round(q(0.9), 3),
+            "min": round(xs[0], 3), "max": round(xs[-1], 3), "samples": len(xs)}
+
+
+def interleaved(torch, stream, fns, n_calls, samples):
+    """FUSED=0/1 style comparison: samples of each fn interleaved in one session."""
+    res = {k: [] for k in fns}
+    for _ in range(samples):
+        for k, fn in fns.items():
+            res[k].extend(sample_calls(torch, stream, fn, n_calls, 1))
+    return res
+
+
+# DRAM bytes per call of the SwiGLU paths from ncu captures (dram__bytes_read.sum +
+# dram__bytes_write.sum summed over the kernels of one call), keyed by the source
+# hash of the kernels and the case; null once the code changes.
+NCU_SWIGLU_BYTES = {}
+
+
+def extras(args, w4, torch, device, stream, l2, checks):
+    """Secondary measurements. Every shape's output is kept (a few rows) in
+    `checks` and compared with the float64 oracle in the CPU-baseline leg."""
+    import numpy as np
+    from w4a16_inputs import draw_norm_weight, make_case, make_swiglu_case
+    hbm_peak, tf_peak, _ = load_peaks()
     res = {}
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
 
     def weights(case, copies_min=4):
-        q = w4.w4a16_repack(torch.from_numpy(case.bq).to(device))
-        s = torch.from_numpy(case.scales).to(device)
-        z = None if case.zp is None else torch.from_numpy(case.zp).to(device)
+        q = w4.w4a16_repack(dev(case.bq))
+        s = dev(case.scales)
+        z = None if case.zp is None else dev(case.zp)
         wb = q.numel() + s.numel() * s.element_size() + (0 if z is None else z.numel())
         n = max(copies_min, math.ceil(3 * l2 / wb))
-        return [(q, s, z)] + [(q.clone(), s.clone(), None if z is None else z.clone())
-                              for _ in range(n - 1)]
+        return [(q, s, z)] + [(q.clone(), s.clone(), None if z is None else z.clone()) for _ in range(n - 1)]
 
-    for name, (Kx, Nx, Ms) in {"mlp": (5120, 13824, (1, 2, 4, 8, 16, 32, 64)),
-                               "decode": (4096, 4096, (1, 2, 4, 8))}.items():
-        base = make_case(max(Ms), Nx, Kx, 128, seed=2 if name == "mlp" else 1)
+    def keep(label, Y, kind, case, rows, **kw):
+        checks.append(dict(label=label, y=Y.float().cpu().double().numpy()[rows], kind=kind, case=case,
+                           rows=list(rows), **kw))
+
+    # -- small-M GEMM sweeps, launch overlap off and on (interleaved samples)
+    for name, (Kx, Nx, Ms, seed) in {"mlp": (5120, 13824, (1, 2, 4, 8, 16, 32, 64), 2),
+                                     "decode": (4096, 4096, (1, 2, 4, 8), 1)}.items():
+        base = make_case(max(Ms), Nx, Kx, 128, seed=seed)
         rot = weights(base)
         rows = {}
         for m in Ms:
-            A = torch.from_numpy(base.A[:m].copy()).to(device)
+            A = dev(base.A[:m])
             Yx = torch.empty((m, Nx), dtype=torch.float16, device=device)
 
             def fn(i, A=A, Yx=Yx):
                 q, s, z = rot[i % len(rot)]
                 w4.w4a16_gemm(A, q, s, z, 128, out=Yx, stream=stream)
-            us = time_calls(torch, stream, fn, 200, reps=5)
+            smp = {False: [], True: []}
+            for _ in range(5):
+                for on in (False, True):
+                    w4.w4a16_set_launch_overlap(on)
+                    smp[on].append(time_calls(torch, stream, fn, 200))
+            w4.w4a16_set_launch_overlap(False)
+            fn(0)
+            torch.cuda.synchronize()
+            keep(f"{name} M={m}", Yx, "gemm", base, sorted({0, m - 1}), m=m)
             b = algorithmic_bytes(m, Nx, Kx, 128)
+            off_us, on_us = statistics.median(smp[False]), statistics.median(smp[True])
             path, split = w4.w4a16_gemm_plan(m, Nx, Kx, 128)
-            rows[f"M={m}"] = {"us": round(us, 3), "GB/s": round(b / us / 1e3, 1),
-                              "hbm_frac": round(b / us / 1e3 / hbm_peak, 3), "split_k": split,
-                              "path": ["small_m", "tcgen05"][path]}
+            rows[f"M={m}"] = {"us": round(off_us, 3), "us_launch_overlap": round(on_us, 3),
+                              "hbm_frac": round(b / off_us / 1e3 / hbm_peak, 3),
+                              "hbm_frac_launch_overlap": round(b / on_us / 1e3 / hbm_peak, 3),
+                              "split_k": split, "path": ["small_m", "tcgen05"][path]}
         res[name] = rows
         del rot
 
-    # Launch overlap (programmatic dependent launch) off vs on, interleaved samples.
-    base = make_case(32, 13824, 5120, 128, seed=2)
-    rot = weights(base)
-    ov = {}
-    for m in (1, 8, 32):
-        A = torch.from_numpy(base.A[:m].copy()).to(device)
-        Yx = torch.empty((m, 13824), dtype=torch.float16, device=device)
-
-        def fn(i, A=A, Yx=Yx):
-            q, s, z = rot[i % len(rot)]
-            w4.w4a16_gemm(A, q, s, z, 128, out=Yx, stream=stream)
-        smp = {False: [], True: []}
-        for _ in range(5):
-            for on in (False, True):
-                w4.w4a16_set_launch_overlap(on)
-                smp[on].append(time_calls(torch, stream, fn, 200))
-        w4.w4a16_set_launch_overlap(False)
-        b = algorithmic_bytes(m, 13824, 5120, 128)
-        off_us, on_us = statistics.median(smp[False]), statistics.median(smp[True])
-        ov[f"M={m}"] = {"off_us": round(off_us, 3), "on_us": round(on_us, 3),
-                        "on_hbm_frac": round(b / on_us / 1e3 / hbm_peak, 3)}
-    res["mlp_launch_overlap"] = ov
-    del rot
-
-    # SwiGLU fused vs unfused at decode M (interleaved samples, same buffers).
+    # -- SwiGLU fused vs unfused at decode M: >= 20 interleaved samples each
     gc, uc = make_swiglu_case(8, 13824, 5120, 128, seed=4)
-    A = torch.from_numpy(gc.A).to(device)
-    gq = w4.w4a16_repack(torch.from_numpy(gc.bq).to(device))
-    uq = w4.w4a16_repack(torch.from_numpy(uc.bq).to(device))
-    tens = [torch.from_numpy(x).to(device) for x in (gc.scales, gc.zp, uc.scales, uc.zp)]
-    n_pair = max(3, math.ceil(3 * l2 / (2 * gq.numel())))
-    sets = [(gq, uq)] + [(gq.clone(), uq.clone()) for _ in range(n_pair - 1)]
+    A = dev(gc.A)
+    grot, urot = weights(gc, 2), weights(uc, 2)
+    npair = min(len(grot), len(urot))
     Yx = torch.empty((8, 13824), dtype=torch.float16, device=device)
-    ws = torch.empty(w4.w4a16_swiglu_workspace_bytes(8, 13824, 5120, 128, 0), dtype=torch.uint8,
-                     device=device)
-    samples = {True: [], False: []}
-    for _ in range(5):
-        for fused in (True, False):
-            def fn(i, fused=fused):
-                g_, u_ = sets[i % n_pair]
-                w4.w4a16_gemm_swiglu(A, g_, tens[0], tens[1], u_, tens[2], tens[3], 128,
-                                     fused=fused, out=Yx, workspace=ws, stream=stream)
-            samples[fused].append(time_calls(torch, stream, fn, 100))
-    # Fused: two weight sets, A read once, Y written once.
-    b_fused = 2 * (algorithmic_bytes(8, 13824, 5120, 128) - 2 * 8 * 5120 - 2 * 8 * 13824) \
-        + 2 * 8 * 5120 + 2 * 8 * 13824
-    res["swiglu_M8"] = {
-        "fused_us": round(statistics.median(samples[True]), 3),
-        "unfused_us": round(statistics.median(samples[False]), 3),
-        "analytic_delta_bytes": 8 * 8 * 13824,
-        "delta_note": "upper bound from shape, DRAM level: unfused writes G,U (4MN), reads them "
-                      "back (4MN); fused writes only Y",
-        "fused_GB/s": round(b_fused / statistics.median(samples[True]) / 1e3, 1),
-    }
-    del sets
+    ws = torch.empty(w4.w4a16_swiglu_workspace_bytes(8, 13824, 5120, 128, 0), dtype=torch.uint8, device=device)
+    fns = {}
+    for fused in (True, False):
+        def fn(i, fused=fused):
+            (gq, gs, gz), (uq, us_, uz) = grot[i % npair], urot[i % npair]
+            w4.w4a16_gemm_swiglu(A, gq, gs, gz, uq, us_, uz, 128, fused=fused, out=Yx, workspace=ws,
+                                 stream=stream)
+        fns["fused" if fused else "unfused"] = fn
+    for ov in (False, True):
+        w4.w4a16_set_launch_overlap(ov)
+        smp = interleaved(torch, stream, fns, 50, 20)
+        key = "swiglu_M8" + ("_launch_overlap" if ov else "")
+        b_fused = 2 * algorithmic_bytes(8, 13824, 5120, 128) - 2 * 8 * 5120 - 2 * 8 * 13824
+        b_unfused = b_fused + 8 * 8 * 13824
+        res[key] = {
+            "fused_us": spread(smp["fused"]), "unfused_us": spread(smp["unfused"]),
+            "analytic_bytes": {"fused": b_fused, "unfused": b_unfused, "delta": 8 * 8 * 13824,
+                               "note": "upper bound from shape, DRAM level: unfused writes G,U (4MN) and reads "
+                                       "them back (4MN); fused writes only Y"},
+            "algorithmic_GB/s": {"fused": round(b_fused / statistics.median(smp["fused"]) / 1e3, 1),
+                                 "unfused": round(b_unfused / statistics.median(smp["unfused"]) / 1e3, 1)},
+            "measured_dram_bytes": NCU_SWIGLU_BYTES.get(("M=8", kernel_source_hash())),
+        }
+    w4.w4a16_set_launch_overlap(False)
+    fns["fused"](0)
+    torch.cuda.synchronize()
+    keep("swiglu fused M=8", Yx, "swiglu", (gc, uc), [0, 7])
+    fns["unfused"](0)
+    torch.cuda.synchronize()
+    keep("swiglu unfused M=8", Yx, "swiglu", (gc, uc), [0, 7])
+    del grot, urot
 
-    # Tensor-core regime: MLP GEMM at larger M and the gate/up SwiGLU (fused vs unfused).
-    _, tf_peak, _ = load_peaks()
-    base = make_case(8, 13824, 5120, 128, seed=2)
-    rot = weights(base, copies_min=2)
+    # -- tensor-core regime: plain GEMM at large M (roofline against the bf16 peak)
+    base = make_case(4096, 13824, 5120, 128, seed=2)
+    rot = weights(base, 2)
     rows = {}
     for m in (128, 256, 1024, 4096):
-        A = torch.randn((m, 5120), device=device).half()
+        A = dev(base.A[:m])
         Yx = torch.empty((m, 13824), dtype=torch.float16, device=device)
 
         def fn(i, A=A, Yx=Yx):
             q, s_, z = rot[i % len(rot)]
             w4.w4a16_gemm(A, q, s_, z, 128, out=Yx, stream=stream)
         n = max(4, int(2000 / m))
-        us = time_calls(torch, stream, fn, n, reps=3)
+        smp = sample_calls(torch, stream, fn, n, 7)
+        us = statistics.median(smp)
         tflops = 2 * m * 13824 * 5120 / us / 1e6
-        rows[f"M={m}"] = {"us": round(us, 2), "TFLOP/s": round(tflops, 1),
-                          "tensor_frac": round(tflops / tf_peak, 3),
+        fn(0)
+        torch.cuda.synchronize()
+        keep(f"mlp_large_m M={m}", Yx, "gemm", base, sorted({0, m // 2, m - 1}), m=m)
+        rows[f"M={m}"] = {"us": spread(smp), "TFLOP/s": round(tflops, 1), "tensor_frac": round(tflops / tf_peak, 3),
                           "path": ["small_m", "tcgen05"][w4.w4a16_gemm_plan(m, 13824, 5120, 128)[0]]}
     res["mlp_large_m"] = rows
     del rot
 
-    gc, uc = make_swiglu_case(8, 13824, 5120, 128, seed=4)
-    gq = w4.w4a16_repack(torch.from_numpy(gc.bq).to(device))
-    uq = w4.w4a16_repack(torch.from_numpy(uc.bq).to(device))
-    tens = [torch.from_numpy(x).to(device) for x in (gc.scales, gc.zp, uc.scales, uc.zp)]
+    # -- gate/up SwiGLU at prefill M, fused vs unfused (>= 20 interleaved samples)
+    gc, uc = make_swiglu_case(8192, 13824, 5120, 128, seed=4)
+    grot, urot = weights(gc, 3), weights(uc, 3)
+    npair = min(len(grot), len(urot))
     rows = {}
     for m in (256, 1024, 4096, 8192):
-        A = torch.randn((m, 5120), device=device).half()
+        A = dev(gc.A[:m])
         Yx = torch.empty((m, 13824), dtype=torch.float16, device=device)
         ws = torch.empty(w4.w4a16_swiglu_workspace_bytes(m, 13824, 5120, 128, 0), dtype=torch.uint8,
                          device=device)
-        samples = {True: [], False: []}
-        n = max(2, int(1000 / m))
-        for _ in range(3):
-            for fused in (True, False):
-                def fn(i, fused=fused, A=A, Yx=Yx, ws=ws):
-                    w4.w4a16_gemm_swiglu(A, gq, tens[0], tens[1], uq, tens[2], tens[3], 128,
-                                         fused=fused, out=Yx, workspace=ws, stream=stream)
-                samples[fused].append(time_calls(torch, stream, fn, n))
-        fu, un = statistics.median(samples[True]), statistics.median(samples[False])
+        fns = {}
+        for fused in (True, False):
+            def fn(i, fused=fused, A=A, Yx=Yx, ws=ws):
+                (gq, gs, gz), (uq, us_, uz) = grot[i % npair], urot[i % npair]
+                w4.w4a16_gemm_swiglu(A, gq, gs, gz, uq, us_, uz, 128, fused=fused, out=Yx, workspace=ws,
+                                     stream=stream)
+            fns["fused" if fused else "unfused"] = fn
+        smp = interleaved(torch, stream, fns, max(2, 1024 // m), 20)
+        fu, un = statistics.median(smp["fused"]), statistics.median(smp["unfused"])
         flops = 4 * m * 13824 * 5120
-        rows[f"M={m}"] = {"fused_us": round(fu, 1), "unfused_us": round(un, 1),
+        for k in ("fused", "unfused"):
+            fns[k](0)
+            torch.cuda.synchronize()
+            keep(f"gate_up {k} M={m}", Yx, "swiglu", (gc, uc), sorted({0, m // 2, m - 1}), m=m)
+        rows[f"M={m}"] = {"fused_us": spread(smp["fused"]), "unfused_us": spread(smp["unfused"]),
                           "fused_TFLOP/s": round(flops / fu / 1e6, 1),
                           "fused_tensor_frac": round(flops / fu / 1e6 / tf_peak, 3),
+                          "unfused_TFLOP/s": round(flops / un / 1e6, 1),
                           "analytic_delta_bytes": 8 * m * 13824,
                           "delta_note": "upper bound from shape, DRAM level"}
         del ws
     res["gate_up_swiglu"] = rows
 
-    # Repack (one-time): read N*K/2 + write N*K/2 bytes.
+    # -- MLP chain: gate/up SwiGLU (K=5120, N=13824) -> down projection (K=13824, N=5120)
+    dc = make_case(8, 5120, 13824, 128, seed=5)
+    drot = weights(dc, 2)
+    rows = {}
+    for m in (8, 1024):
+        A = dev(gc.A[:m])
+        H = torch.empty((m, 13824), dtype=torch.float16, device=device)
+        Yx = torch.empty((m, 5120), dtype=torch.float16, device=device)
+        ws = torch.empty(w4.w4a16_swiglu_workspace_bytes(m, 13824, 5120, 128, 0), dtype=torch.uint8,
+                         device=device)
+        fns = {}
+        for fused in (True, False):
+            def fn(i, fused=fused, A=A, H=H, Yx=Yx, ws=ws):
+                (gq, gs, gz), (uq, us_, uz) = grot[i % npair], urot[i % npair]
+                w4.w4a16_gemm_swiglu(A, gq, gs, gz, uq, us_, uz, 128, fused=fused, out=H, workspace=ws,
+                                     stream=stream)
+                dq, ds, dz = drot[i % len(drot)]
+                w4.w4a16_gemm(H, dq, ds, dz, 128, out=Yx, stream=stream)
+            fns["fused" if fused else "unfused"] = fn
+        smp = interleaved(torch, stream, fns, max(2, 200 // m), 20)
+        for k in ("fused", "unfused"):
+            fns[k](0)
+            torch.cuda.synchronize()
+            keep(f"mlp_chain {k} M={m}", Yx, "chain", (gc, uc, dc), sorted({0, m - 1}), m=m)
+        b = 2 * algorithmic_bytes(m, 13824, 5120, 128) + algorithmic_bytes(m, 5120, 13824, 128)
+        rows[f"M={m}"] = {"fused_us": spread(smp["fused"]), "unfused_us": spread(smp["unfused"]),
+                          "bytes_per_chain": b, "flops_per_chain": 6 * m * 13824 * 5120}
+        del ws
+    res["mlp_chain"] = rows
+    del grot, urot, drot
+
+    # -- RMS-norm prologue: staged normalisation + GEMM, against the plain GEMM
+    base = make_case(8, 13824, 5120, 128, seed=2)
+    rot = weights(base)
+    gamma = dev(draw_norm_weight(np.random.default_rng(9), 5120))
+    A = dev(base.A)
+    Yx = torch.empty((8, 13824), dtype=torch.float16, device=device)
+    wsn = torch.empty(w4.w4a16_rmsnorm_workspace_bytes(8, 13824, 5120, 128, 0), dtype=torch.uint8, device=device)
+    fns = {"plain": lambda i: w4.w4a16_gemm(A, *rot[i % len(rot)][:2], rot[i % len(rot)][2], 128, out=Yx,
+                                            stream=stream),
+           "rmsnorm": lambda i: w4.w4a16_gemm_rmsnorm(A, gamma, 1e-5, *rot[i % len(rot)], 128, out=Yx,
+                                                      workspace=wsn, stream=stream)}
+    r = {}
+    for ov in (False, True):
+        w4.w4a16_set_launch_overlap(ov)
+        smp = interleaved(torch, stream, fns, 100, 10)
+        r["launch_overlap" if ov else "plain_launch"] = {k: spread(v) for k, v in smp.items()}
+    w4.w4a16_set_launch_overlap(False)
+    fns["rmsnorm"](0)
+    torch.cuda.synchronize()
+    keep("rmsnorm gemm M=8", Yx, "rmsnorm", base, [0, 7], gamma=gamma.cpu().numpy(), eps=1e-5)
+    res["rmsnorm_M8"] = r
+    del rot
+
+    # -- repack (one-time): read N*K/2 + write N*K/2 bytes
     qsrc = torch.randint(0, 256, (13824, 2560), dtype=torch.uint8, device=device)
     qdst = torch.empty(13824 * 2560, dtype=torch.uint8, device=device)
     us = time_calls(torch, stream, lambda i: w4.w4a16_repack(qsrc, out=qdst, stream=stream), 20)
-    res["repack_13824x5120"] = {"us": round(us, 2),
-                                "GB/s": round(2 * qsrc.numel() / us / 1e3, 1)}
+    res["repack_13824x5120"] = {"us": round(us, 2), "GB/s": round(2 * qsrc.numel() / us / 1e3, 1)}
     return res
+
+
+def check_parity(checks):
+    """Oracle comparison of the kept rows (CPU-baseline leg): max|Y - Y_ref| <=
+    2e-2 * max|Y_ref| per shape, worst errors reported."""
+    import numpy as np
+    import oracle
+    out, ok = {}, True
+    for c in checks:
+        rows = c["rows"]
+        if c["kind"] == "gemm":
+            cs = c["case"]
+            ref = oracle.gemm(cs.A[:c.get("m", cs.M)], cs.bq, cs.scales, cs.zp, cs.group, rows=rows)
+        elif c["kind"] == "rmsnorm":
+            cs = c["case"]
+            ref = oracle.gemm_rmsnorm(cs.A, c["gamma"], c["eps"], cs.bq, cs.scales, cs.zp, cs.group, rows=rows)
+        elif c["kind"] == "swiglu":
+            g, u = c["case"]
+            ref = oracle.gemm_swiglu(g.A[:c.get("m", g.M)], (g.bq, g.scales, g.zp), (u.bq, u.scales, u.zp),
+                                     g.group, rows=rows)
+        else:  # chain: swiglu -> down, composed in float64
+            g, u, d = c["case"]
+            h = oracle.gemm_swiglu(g.A[:c.get("m", g.M)], (g.bq, g.scales, g.zp), (u.bq, u.scales, u.zp),
+                                   g.group, rows=rows)
+            ref = oracle.gemm(h, d.bq, d.scales, d.zp, d.group)
+        err = float(np.abs(c["y"] - ref).max())
+        tol = 2e-2 * float(np.abs(ref).max())
+        ok = ok and err <= tol
+        out[c["label"]] = {"worst_abs": round(err, 5), "tol": round(tol, 5), "pass": err <= tol}
+    return ok, out
 
 
 SINGLE_CASES = {

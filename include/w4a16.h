@@ -70,14 +70,14 @@ size_t w4a16_repacked_bytes(int N, int K);
  * kernels read (the MatMulNBits pull request's "bijective ... reorder for
  * coalesced loads" with a device repack byte-identical to a host reference; the
  * permutation itself is this library's own):
- *   row tile n0 = 128*(n/128) with R = min(128, N-n0) rows; k-block b = k/64;
- *   chunk (tile, b) = R*32 bytes at n0*K/2 + b*R*32; inside it 16-row sub-tile
- *   s = (n-n0)/16 at s*512; with g = (n-n0)%8 and t = (k%16)/4 the 16-byte lane
- *   slot 4*g + (t + g/2)%4 at slot*16; u32 word j = (k%64)/16 at j*4; nibble
- *   p = 4*(e%2) + 2*(e/2) + h with e = k%4 and h = ((n-n0)%16)/8 (byte p/2 of the
- *   word, high nibble when p is odd). Each lane slot is one mma.sync m16n8k16
- *   A fragment per word (rows g and g+8); a 16-row x 64-k sub-tile is 512
- *   contiguous bytes and a (tile, k-block) chunk one contiguous bulk copy.
+ *   16-row sub-tile S = n/16, k-block b = k/64: piece (S, b) is 512 bytes at
+ *   (S*(K/64) + b)*512, so every sub-tile is one contiguous run along K and a run
+ *   of k-blocks of consecutive sub-tiles is a regular 3-D box for TMA copies;
+ *   with g = n%8 and t = (k%16)/4 the 16-byte lane slot 4*g + (t + g/2)%4 of the
+ *   piece at slot*16; u32 word j = (k%64)/16 at j*4; nibble p = 4*(e%2) + 2*(e/2)
+ *   + h with e = k%4 and h = (n%16)/8 (byte p/2 of the word, high nibble when p
+ *   is odd). Each lane slot holds one mma.sync m16n8k16 A fragment per word
+ *   (rows g and g+8).
  *   q      device, uint8 [N][K/2] (input format above); not modified
  *   q_rep  device, w4a16_repacked_bytes(N, K) bytes, written; must not overlap q
  * Integer-only and bit-exact; inverse: w4a16_unpack_host.
@@ -117,15 +117,17 @@ w4a16_status w4a16_gemm_plan(int M, int N, int K, int group, int split_k,
  *   zp       device uint8 [N][ceil(G/2)] packed zero points, or NULL (zero point 8)
  *   Y        device fp16 [M][N], written (no read-modify-write)
  *   split_k  0 = automatic; 1..8 forces the small-M path's K split (a cluster
- *            of that many CTAs per 128-row tile) for M up to the small-M limit;
- *            ignored on the tensor-core path
+ *            of that many CTAs along K per run of sub-tiles) for M up to the
+ *            small-M limit; ignored on the tensor-core path
  *   ws, ws_bytes  caller scratch of at least w4a16_gemm_workspace_bytes(); may be
  *            NULL when that is 0
- * Small M (see w4a16_gemm_plan for the choice) runs the stream kernel: weights
- * streamed by bulk copies through a shared-memory ring, dequantisation in
- * registers, mma.sync m16n8k16 with fp32 accumulation and the group scale applied
- * after each group's partial sum (the pull request's "per-group scale AFTER the
- * tensor-core accumulate"), K split across a cluster and reduced in a fixed order.
+ * Small M (see w4a16_gemm_plan for the choice) runs the stream kernel: weight
+ * and activation boxes streamed by TMA through a shared-memory ring, each CTA a
+ * run of 16-row sub-tiles over a K range, dequantisation in registers,
+ * mma.sync m16n8k16 with fp32 accumulation and the group scale applied after
+ * each group's partial sum (the pull request's "per-group scale AFTER the
+ * tensor-core accumulate"); when the row split alone cannot fill the GPU, K is
+ * split across a cluster and reduced in a fixed order.
  * Larger M runs the tcgen05 kernel: TMA-staged activations, int4 tiles dequantised to fp16
  * ((q - zp) * scale rounded once; fp32 scales are rounded to fp16 first) into
  * tensor memory, fp32 accumulation in tensor memory.
@@ -157,6 +159,36 @@ w4a16_status w4a16_gemm_swiglu(const uint16_t *A,
                                w4a16_scale_dtype sdt, uint16_t *Y,
                                int M, int N, int K, int group, int fused,
                                void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * RMS-norm prologue (the pull request's "Update -- fused RMS-norm epilogue + e2e
+ * PASS" and "Update -- P1 COMPLETE": the normalised activation is staged in
+ * scratch, then the GEMM runs on it; gate_up SwiGLU has the same optional
+ * prologue). The pages give no formula; the reading taken is the ONNX
+ * SimplifiedLayerNormalization that the prologue replaces:
+ *     An[m,k] = A[m,k] / sqrt(mean_k A[m,k]^2 + eps) * gamma[k]
+ * computed in fp32 per row (fixed-order sum of squares) and stored as fp16 in
+ * the caller's workspace; the GEMM (or SwiGLU) then runs on An exactly as
+ * w4a16_gemm (w4a16_gemm_swiglu) would. With launch overlap on, the GEMM is a
+ * programmatic dependent of the prologue and streams weights while it runs.
+ *   gamma    device fp16 [K], 16-byte aligned
+ *   eps      >= 0 (finite)
+ *   ws       device scratch of w4a16_rmsnorm_workspace_bytes(M, N, K, group,
+ *            mode) bytes, 256-byte aligned; mode 0 = w4a16_gemm_rmsnorm,
+ *            1 = fused SwiGLU, 2 = unfused SwiGLU (An followed by the unfused
+ *            chain's intermediates). Too small -> W4A16_ERR_WORKSPACE.
+ * Other arguments, layouts and errors as w4a16_gemm / w4a16_gemm_swiglu.
+ */
+size_t w4a16_rmsnorm_workspace_bytes(int M, int N, int K, int group, int mode);
+w4a16_status w4a16_gemm_rmsnorm(const uint16_t *A, const uint16_t *gamma, float eps, const uint8_t *q_rep,
+                                const void *scales, w4a16_scale_dtype sdt, const uint8_t *zp, uint16_t *Y,
+                                int M, int N, int K, int group, int split_k, void *ws, size_t ws_bytes,
+                                void *stream);
+w4a16_status w4a16_gemm_swiglu_rmsnorm(const uint16_t *A, const uint16_t *gamma, float eps,
+                                       const uint8_t *qg_rep, const void *sg, const uint8_t *zg,
+                                       const uint8_t *qu_rep, const void *su, const uint8_t *zu,
+                                       w4a16_scale_dtype sdt, uint16_t *Y, int M, int N, int K, int group,
+                                       int fused, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Unfused SwiGLU (as w4a16_gemm_swiglu with fused = 0) for callers that cannot

@@ -13,15 +13,17 @@ layout, stated here as an index map from a logical nibble (n, k) of Bq[N][K/2]
 (byte k/2 of row n, low nibble for even k) to a (byte, nibble) position of the
 repacked buffer, which has the same N*K/2 bytes:
 
-    row tile   n0 = 128*(n // 128),  R = min(128, N - n0)   (rows in the tile)
+    sub-tile   S  = n // 16                                (16 weight rows)
     k-block    b  = k // 64
-    chunk      starts at byte n0*K/2 + b*R*32, spans R*32 bytes
-    sub-tile   s  = (n - n0) // 16                         -> s*512 within the chunk
-    lane slot  l  = 4*g + (t + g//2) % 4,  g = (n - n0) % 8,  t = (k % 16) // 4   -> l*16
+    piece      (S, b) starts at byte (S*(K/64) + b)*512, spans 512 bytes
+    lane slot  l  = 4*g + (t + g//2) % 4,  g = n % 8,  t = (k % 16) // 4   -> l*16
     word       j  = (k % 64) // 16                         -> j*4 (little-endian u32)
-    nibble     p  = 4*(e % 2) + 2*(e // 2) + h,  e = k % 4,  h = ((n - n0) % 16) // 8
+    nibble     p  = 4*(e % 2) + 2*(e // 2) + h,  e = k % 4,  h = (n % 16) // 8
                byte j*4 + p//2 of the lane, high nibble when p is odd
 
+So every 16-row sub-tile is one contiguous span of K/64 pieces, and a run of
+consecutive k-blocks of consecutive sub-tiles is a regular 3-D box
+(512-byte pieces x k-blocks x sub-tiles) for a tensor-memory-access copy.
 N must be a multiple of 16 and K a multiple of 64.
 
 Reading of the layout (what the two GPU consumers rely on; the tests check both
@@ -49,20 +51,16 @@ def nibble_position(n, k, N: int, K: int):
     """Vectorised index map: logical nibble (n, k) -> (byte offset, is_high_nibble)."""
     n = np.asarray(n, dtype=np.int64)
     k = np.asarray(k, dtype=np.int64)
-    n0 = 128 * (n // 128)
-    R = np.minimum(128, N - n0)
+    S = n // 16
     b = k // 64
-    chunk = n0 * (K // 2) + b * R * 32
-    r = n - n0
-    s = r // 16
-    g = r % 8
-    h = (r % 16) // 8
+    g = n % 8
+    h = (n % 16) // 8
     t = (k % 16) // 4
     j = (k % 64) // 16
     e = k % 4
     lane = 4 * g + (t + g // 2) % 4
     p = 4 * (e % 2) + 2 * (e // 2) + h
-    byte = chunk + s * 512 + lane * 16 + j * 4 + p // 2
+    byte = (S * (K // 64) + b) * 512 + lane * 16 + j * 4 + p // 2
     return byte, (p % 2).astype(bool)
 
 

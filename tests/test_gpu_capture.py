@@ -9,7 +9,7 @@ in torch's global capture mode, which fails the capture if anything in the
 process makes a call that is unsafe during capture. The tests check
   * the device's free memory is the same before and after eager calls and graph
     replays (the library itself never allocates device memory);
-  * torch's allocator statistics do not move while the library is captured;
+  * capture in global mode succeeds (no synchronising or otherwise unsafe call);
   * two replays give output byte-identical to the eager call.
 Covered: w4a16_gemm on the small-M and tensor-core paths (plain launches and
 launch overlap), w4a16_gemm_swiglu fused and unfused on both paths.
@@ -50,12 +50,9 @@ def capture_and_replay(fn, out):
     torch.cuda.current_stream().wait_stream(stream)
     assert free_bytes() == before, "eager calls changed the device's free memory"
 
-    stats0 = torch.cuda.memory_stats().get("allocation.all.allocated", 0)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream, capture_error_mode="global"):
         fn()
-    stats1 = torch.cuda.memory_stats().get("allocation.all.allocated", 0)
-    assert stats1 == stats0, "an allocation went through torch during capture"
 
     out.zero_()
     torch.cuda.synchronize()

@@ -145,7 +145,9 @@ def test_large_mean_and_magnitude_activations(gpu_lib, path, mean, std, M, N, K,
     c = make_case(M, N, K, group, seed=3 * M + K)
     A = large_mean(M, K, seed=M, mean=mean, std=std)
     ref = oracle.gemm(A, c.bq, c.scales, c.zp, group)
-    assert np.abs(ref).max() < 6e4  # representable in fp16
+    while np.abs(ref).max() >= 3e4:  # keep Y inside fp16: halve A (exact) until it is
+        A = (A.astype(np.float32) * 0.5).astype(np.float16)
+        ref = oracle.gemm(A, c.bq, c.scales, c.zp, group)
     check(gemm(w4, A, c.bq, c.scales, c.zp, group), ref,
           f"{path} A~N({mean},{std}) {M}x{N}x{K} g={group}")
 

@@ -49,7 +49,9 @@ def expire_then_recover(w4, call, ref):
     assert err <= 2e-2 * np.abs(ref).max(), err
 
 
-@pytest.mark.parametrize("M,N,K,split", [(8, 13824, 5120, 0), (8, 2048, 2048, 1), (1, 4096, 4096, 8)])
+# Shapes whose CTAs stream more pipeline stages than their ring holds, so that
+# later stages are certainly still in flight when a consumer first polls them.
+@pytest.mark.parametrize("M,N,K,split", [(8, 13824, 5120, 0), (8, 4096, 14336, 1), (1, 4096, 28672, 8)])
 def test_small_m_wait_expiry(w4, M, N, K, split):
     c = make_case(M, N, K, 128, seed=70 + M)
     A, q, s, z = dev(c.A), w4.w4a16_repack(dev(c.bq)), dev(c.scales), dev(c.zp)
@@ -78,9 +80,9 @@ def test_tcgen05_wait_expiry(w4, M, N):
     assert np.abs(y[rows] - ref).max() <= 2e-2 * np.abs(ref).max()
 
 
-@pytest.mark.parametrize("M", [8, 300])
-def test_swiglu_fused_wait_expiry(w4, M):
-    gc, uc = make_swiglu_case(M, 1024, 2048, 64, seed=90 + M)
+@pytest.mark.parametrize("M,N,K", [(8, 13824, 5120), (300, 1024, 2048)])
+def test_swiglu_fused_wait_expiry(w4, M, N, K):
+    gc, uc = make_swiglu_case(M, N, K, 64, seed=90 + M)
     args = (dev(gc.A), w4.w4a16_repack(dev(gc.bq)), dev(gc.scales), dev(gc.zp),
             w4.w4a16_repack(dev(uc.bq)), dev(uc.scales), dev(uc.zp), 64)
     ref = oracle.gemm_swiglu(gc.A, (gc.bq, gc.scales, gc.zp), (uc.bq, uc.scales, uc.zp), 64)

@@ -101,6 +101,29 @@ def test_swiglu_workspace_validation(w4):
     assert lib.w4a16_gemm_swiglu(*bad, 1, None, 0, None) == w4.W4A16_ERR_INVALID_ARG
 
 
+def test_rmsnorm_validation(w4):
+    lib = w4.lib
+    need = w4.w4a16_rmsnorm_workspace_bytes(8, 256, 512, 64, 0)
+    assert need >= 8 * 512 * 2
+    assert w4.w4a16_rmsnorm_workspace_bytes(8, 256, 512, 64, 2) >= need + 4 * 8 * 256
+    assert w4.w4a16_rmsnorm_workspace_bytes(8, 256, 512, 64, 3) == 0
+    base = dict(A=A16, gamma=A16, eps=1e-5, q=A16, s=A16, sdt=0, zp=None, Y=A16, M=8, N=256, K=512, group=64,
+                split=0, ws=A16 * 16, ws_bytes=need)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return lib.w4a16_gemm_rmsnorm(a["A"], a["gamma"], a["eps"], a["q"], a["s"], a["sdt"], a["zp"], a["Y"],
+                                      a["M"], a["N"], a["K"], a["group"], a["split"], a["ws"], a["ws_bytes"],
+                                      None)
+    assert call(gamma=None) == w4.W4A16_ERR_INVALID_ARG
+    assert call(gamma=BAD) == w4.W4A16_ERR_INVALID_ARG
+    assert call(eps=-1.0) == w4.W4A16_ERR_INVALID_ARG
+    assert call(ws_bytes=need - 1) == w4.W4A16_ERR_WORKSPACE
+    assert call(ws=None) == w4.W4A16_ERR_WORKSPACE
+    assert call(group=48) == w4.W4A16_ERR_UNSUPPORTED
+    assert call(q=None) == w4.W4A16_ERR_INVALID_ARG
+
+
 def test_repack_validation(w4):
     lib = w4.lib
     assert lib.w4a16_repack(A16, 0x20000, 8, 64, None) == w4.W4A16_ERR_UNSUPPORTED

@@ -67,6 +67,18 @@ def test_one_row_per_thread_reads_spread_over_bank_groups():
         assert sorted(_slot(g, t) for t in range(4)) == list(range(4 * g, 4 * g + 4))
 
 
+@pytest.mark.parametrize("N,K", [(32, 128), (144, 192)])
+def test_sub_tile_is_one_contiguous_span(N, K):
+    # Rows 16S..16S+15 occupy exactly bytes [S*8K, (S+1)*8K), k-block b of them
+    # bytes [S*8K + 512b, S*8K + 512(b+1)).
+    for S in range(N // 16):
+        for b in range(K // 64):
+            nn, kk = np.meshgrid(np.arange(16 * S, 16 * S + 16), np.arange(64 * b, 64 * b + 64), indexing="ij")
+            byte, _ = RL.nibble_position(nn, kk, N, K)
+            base = S * (K // 64) * 512 + 512 * b
+            assert byte.min() == base and byte.max() == base + 511
+
+
 def test_rejects_unsupported_dims():
     for N, K in [(8, 64), (16, 32), (20, 64)]:
         with pytest.raises(ValueError):
@@ -74,9 +86,9 @@ def test_rejects_unsupported_dims():
 
 
 def _words(rep, N, K, n0, b, s):
-    """The 32 lanes x 4 u32 words of sub-tile s, k-block b, row tile at n0."""
-    R = min(128, N - n0)
-    base = n0 * (K // 2) + b * R * 32 + s * 512
+    """The 32 lanes x 4 u32 words of the piece of sub-tile (n0 // 16 + s), k-block b."""
+    S = n0 // 16 + s
+    base = (S * (K // 64) + b) * 512
     return rep[base:base + 512].view("<u4").reshape(32, 4)
 
 

@@ -15,6 +15,8 @@ Distributions:
   scales  float32 uniform [0.005, 0.02], shape [N, K/group], stored as float16
           or float32
   zp      uint8 uniform 0..255, shape [N, ceil(G/2)]  (None when symmetric)
+  gamma   float32 uniform [0.5, 1.5] rounded to float16, shape [K] (RMS-norm
+          weight; the pages give no distribution)
 """
 from __future__ import annotations
 
@@ -64,6 +66,11 @@ def draw_weights(rng: np.random.Generator, N: int, K: int, group: int,
     scales = scales.astype(scale_dtype)
     zp = rng.integers(0, 256, size=(N, (G + 1) // 2), dtype=np.uint8) if asym else None
     return bq, scales, zp
+
+
+def draw_norm_weight(rng: np.random.Generator, K: int) -> np.ndarray:
+    """RMS-norm weight gamma [K]: float32 uniform [0.5, 1.5] rounded to float16."""
+    return rng.uniform(0.5, 1.5, size=K).astype(np.float32).astype(np.float16)
 
 
 def make_case(M: int, N: int, K: int, group: int, *, seed: int,

@@ -43,7 +43,8 @@ EXPORTS = (
     "w4a16_gemm_workspace_bytes", "w4a16_gemm_plan", "w4a16_gemm",
     "w4a16_swiglu_workspace_bytes", "w4a16_gemm_swiglu", "w4a16_set_tuning", "w4a16_set_launch_overlap",
     "w4a16_device_error", "w4a16_swiglu_static_scratch_bytes", "w4a16_gemm_swiglu_unfused_static",
-    "w4a16_set_wait_limit_ns",
+    "w4a16_set_wait_limit_ns", "w4a16_rmsnorm_workspace_bytes", "w4a16_gemm_rmsnorm",
+    "w4a16_gemm_swiglu_rmsnorm",
 )
 
 _vp, _ci, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -62,6 +63,11 @@ _sig = {
     "w4a16_set_launch_overlap": (_ci, [_ci]),
     "w4a16_device_error": (_ci, [_vp]),
     "w4a16_set_wait_limit_ns": (_ci, [ctypes.c_ulonglong]),
+    "w4a16_rmsnorm_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci]),
+    "w4a16_gemm_rmsnorm": (_ci, [_vp, _vp, ctypes.c_float, _vp, _vp, _ci, _vp, _vp, _ci, _ci, _ci, _ci, _ci,
+                                 _vp, _sz, _vp]),
+    "w4a16_gemm_swiglu_rmsnorm": (_ci, [_vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _vp,
+                                        _ci, _ci, _ci, _ci, _ci, _vp, _sz, _vp]),
     "w4a16_swiglu_static_scratch_bytes": (_sz, []),
     "w4a16_gemm_swiglu_unfused_static": (_ci, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _vp,
                                                _ci, _ci, _ci, _ci, _vp]),
@@ -178,6 +184,47 @@ def w4a16_gemm_swiglu(A, qg_rep, sg, zg, qu_rep, su, zu, group: int, fused: bool
                                  _ptr(su), _ptr(zu), _scale_dtype(sg), _ptr(out), M, N, K, group,
                                  int(bool(fused)), _ptr(workspace), ws_bytes, _stream(stream)),
            "w4a16_gemm_swiglu")
+    return out
+
+
+def w4a16_rmsnorm_workspace_bytes(M, N, K, group, mode) -> int:
+    return int(lib.w4a16_rmsnorm_workspace_bytes(M, N, K, group, mode))
+
+
+def w4a16_gemm_rmsnorm(A, gamma, eps: float, q_rep, scales, zp, group: int, out=None, split_k: int = 0,
+                       workspace=None, stream=None):
+    """Y = rmsnorm(A; gamma, eps) . dequant(q_rep)^T (normalised A staged in the workspace)."""
+    import torch
+    M, K = A.shape
+    N = scales.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    if workspace is None:
+        workspace = torch.empty(w4a16_rmsnorm_workspace_bytes(M, N, K, group, 0), dtype=torch.uint8,
+                                device=A.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.w4a16_gemm_rmsnorm(_ptr(A), _ptr(gamma), float(eps), _ptr(q_rep), _ptr(scales),
+                                  _scale_dtype(scales), _ptr(zp), _ptr(out), M, N, K, group, split_k,
+                                  _ptr(workspace), ws_bytes, _stream(stream)), "w4a16_gemm_rmsnorm")
+    return out
+
+
+def w4a16_gemm_swiglu_rmsnorm(A, gamma, eps: float, qg_rep, sg, zg, qu_rep, su, zu, group: int,
+                              fused: bool = True, out=None, workspace=None, stream=None):
+    """Y = silu(An . Wg^T) * (An . Wu^T), An = rmsnorm(A; gamma, eps)."""
+    import torch
+    M, K = A.shape
+    N = sg.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    if workspace is None:
+        workspace = torch.empty(w4a16_rmsnorm_workspace_bytes(M, N, K, group, 1 if fused else 2),
+                                dtype=torch.uint8, device=A.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.w4a16_gemm_swiglu_rmsnorm(_ptr(A), _ptr(gamma), float(eps), _ptr(qg_rep), _ptr(sg), _ptr(zg),
+                                         _ptr(qu_rep), _ptr(su), _ptr(zu), _scale_dtype(sg), _ptr(out),
+                                         M, N, K, group, int(bool(fused)), _ptr(workspace), ws_bytes,
+                                         _stream(stream)), "w4a16_gemm_swiglu_rmsnorm")
     return out
 
 

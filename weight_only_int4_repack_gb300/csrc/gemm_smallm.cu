@@ -6,15 +6,13 @@
 // occupancy-bound and split the K range over more CTAs, reducing fp32 partials
 // in a fixed order. This kernel keeps those two ideas and re-designs the rest
 // for sm_103a:
-//   * one CTA = one 128-row tile x one K range. In the repacked layout that
-//     range is one contiguous span, so a producer warp streams it through a
-//     shared-memory ring with 16 KB cp.async.bulk copies (four 64-k blocks per
-//     stage). The stream starts once the CTA's scales and zero points have
-//     landed: they gate every group's flush, and issuing weights earlier
-//     measured slower. (Measured on GB300: 1-D bulk copies reach HBM speed with
-//     8-16 KB pieces; with 4 KB pieces a CTA completed only about one copy per
-//     half microsecond.) The K split is chosen per shape so that the busiest SM
-//     streams as few weight bytes as possible;
+//   * one CTA = one 128-row tile (eight 16-row sub-tiles) x one K range. In the
+//     repacked layout four k-blocks of those sub-tiles are one regular 3-D box,
+//     so a producer warp streams the range through a shared-memory ring with one
+//     16 KB TMA copy per stage. The stream starts once the CTA's scales and zero
+//     points have landed: they gate every group's flush, and issuing weights
+//     earlier measured slower. The K split is chosen per shape so that the
+//     busiest SM streams as few weight bytes as possible;
 //   * consumer warps own one or two 16-row sub-tiles; a lane reads one 16-byte
 //     slot per sub-tile and block (a conflict-free 128-bit shared load) whose
 //     four words are mma.sync.m16n8k16 A fragments for four k16 steps; the
@@ -49,8 +47,8 @@ namespace {
 
 constexpr int kPartStride = kTileRows + 4;          // floats per partial row (bank spread)
 constexpr int kBPS = 4;                             // k-blocks per ring stage
-constexpr int kBlkBytes = kTileRows * 32;           // 4 KB: one block slot of a stage
-constexpr int kStageSet = kBlkBytes * kBPS;         // 16 KB: one stage of one weight set
+constexpr int kStageSet = kTileRows * 32 * kBPS;   // 16 KB: one stage of one weight set
+constexpr int kSubStage = kSubBytes * kBPS;         // 2 KB: one sub-tile's four k-blocks in a stage
 
 // Ring stages of kStageSet bytes per weight set: 32 / 64 KB in flight per CTA.
 constexpr int kStages = 2;
@@ -127,7 +125,8 @@ __host__ __device__ inline SmemPlan make_plan(int M, int MT, int group, int kc, 
 
 template <int GROUP, int MT, bool SWIGLU>
 __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>::MINB)
-    smallm_kernel(const SmallMParams p) {
+    smallm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
+                  const SmallMParams p) {
     using Sh = Shape<MT, SWIGLU>;
     constexpr int NS = Sh::NS, SUBT = Sh::SUBT, CW = Sh::CW, STAGES = Sh::STAGES;
     constexpr int NC = CW * 32;                            // consumer threads
@@ -157,7 +156,6 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
     uint64_t *abar = empty + STAGES;  // activation chunk landed
     volatile int *abort_flag = reinterpret_cast<volatile int *>(abar + 1);
     __half *sA = reinterpret_cast<__half *>(smem + plan.a_off);
-    const uint32_t blk_bytes = (uint32_t)R * 32u;  // one (tile, k-block) chunk
 
     // Activations [M][c0*64, c1*64) of a chunk: one bulk copy per token row.
     auto issue_activations = [&](int c0, int c1) {
@@ -255,6 +253,8 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
             };
             if (pre == 0) start_activations();
             const uint64_t stream_policy = ptx::policy_evict_first();
+            ptx::prefetch_tmap(&tm_w0);
+            if (SWIGLU) ptx::prefetch_tmap(&tm_w1);
             int st = 0;
             for (; st < nstage; ++st) {
                 const int s = st % STAGES;
@@ -262,21 +262,12 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                 if (st == pre && !a_issued) start_activations();
                 if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err, p.wait_ns)) break;
                 const int b0 = b_begin + st * kBPS;
-                const uint32_t bytes = blk_bytes * (uint32_t)min(kBPS, b_end - b0);
-                ptx::mbar_arrive_expect_tx(&full[s], NS * bytes);
-                const size_t off = chunk_offset(n0, p.N, p.K, b0);
-#pragma unroll
-                for (int w = 0; w < NS; ++w) {
-                    unsigned char *dst = smem + (size_t)(s * NS + w) * kStageSet;
-                    if (R == kTileRows) {  // full tile: the stage's blocks are one contiguous span
-                        ptx::bulk_g2s_hint(dst, p.w[w].q_rep + off, bytes, &full[s], stream_policy);
-                    } else {               // ragged last tile: one copy per 4 KB block slot
-                        const int nb = min(kBPS, b_end - b0);
-                        for (int i = 0; i < nb; ++i)
-                            ptx::bulk_g2s_hint(dst + i * kBlkBytes, p.w[w].q_rep + off + (size_t)i * blk_bytes,
-                                               blk_bytes, &full[s], stream_policy);
-                    }
-                }
+                // One box: kBPS k-blocks of the tile's eight sub-tiles (sub-tiles past N
+                // and k-blocks past K read as zero), [sub-tile][k-block][512 bytes].
+                ptx::mbar_arrive_expect_tx(&full[s], NS * kStageSet);
+                unsigned char *dst = smem + (size_t)s * NS * kStageSet;
+                ptx::tma_load_3d_hint(dst, &tm_w0, 0, b0, n0 / kSubRows, &full[s], stream_policy);
+                if (SWIGLU) ptx::tma_load_3d_hint(dst + kStageSet, &tm_w1, 0, b0, n0 / kSubRows, &full[s], stream_policy);
             }
             if (!a_issued && !*abort_flag) start_activations();
             if (*abort_flag) {
@@ -408,7 +399,7 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                 // Per-stage bases: every offset below them is a compile-time constant
                 // (weights sit in fixed 4 KB block slots, stages start on a group).
                 const unsigned char *wbase =
-                    smem + (size_t)s * NS * kStageSet + (warp * SUBT) * kSubBytes + slot * 16;
+                    smem + (size_t)s * NS * kStageSet + (warp * SUBT) * kSubStage + slot * 16;
                 const __half *abase = sA + (bs - c0) * kKBlock + 4 * t;
                 const float2 *mbase = meta0 + ((bs - c0) * kKBlock) / GROUP;
                 auto run_stage = [&](auto nbc) {
@@ -420,8 +411,8 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                             constexpr int w = decltype(wc)::value;
                             static_for<0, SUBT>([&](auto uc) {
                                 constexpr int u = decltype(uc)::value;
-                                wv[w][u] = *reinterpret_cast<const uint4 *>(wbase + w * kStageSet + i * kBlkBytes +
-                                                                           u * kSubBytes);
+                                wv[w][u] = *reinterpret_cast<const uint4 *>(wbase + w * kStageSet + u * kSubStage +
+                                                                           i * kSubBytes);
                             });
                         });
                         static_for<0, 4>([&](auto jc) {
@@ -643,7 +634,11 @@ cudaError_t launch_one(const SmallMParams &p, cudaStream_t s) {
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, p);
+    CUtensorMap m0, m1;
+    if (!tmap_weights(&m0, p.w[0].q_rep, p.N, p.K, kBPS, kTileRows / kSubRows)) return cudaErrorInvalidValue;
+    if (!tmap_weights(&m1, p.w[SWIGLU ? 1 : 0].q_rep, p.N, p.K, kBPS, kTileRows / kSubRows))
+        return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(&cfg, kern, m0, m1, p);
 }
 
 template <int GROUP, bool SWIGLU>

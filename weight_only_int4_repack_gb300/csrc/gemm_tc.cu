@@ -30,8 +30,6 @@
 //     silu(gate) * up.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // W4A16_ERR_TIMEOUT, drains what it issued, frees its tensor memory and returns.
-#include <cudaTypedefs.h>
-
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -199,7 +197,8 @@ __device__ __forceinline__ void load_row_meta(const TcParams &p, int w, int n, i
 
 template <int GROUP, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcParams p, int T) {
+    tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w0,
+              const __grid_constant__ CUtensorMap tmap_w1, const TcParams p, int T) {
     using Sh = TcShape;
     constexpr int NS = Sh::NS, STAGES = Sh::STAGES, ASTAGES = Sh::ASTAGES;
     constexpr int COLS = SWIGLU ? 64 : kTileRows;  // output columns per CTA
@@ -221,8 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int m0 = blockIdx.x * T;
     const int n0 = blockIdx.y * COLS;               // first output column
     const int R = min(COLS, p.N - n0);              // output columns of this CTA
-    const int nt0 = n0 / kTileRows * kTileRows;     // repacked tile holding them
-    const uint32_t half_off = (uint32_t)(n0 - nt0) / kSubRows * kSubBytes;  // SwiGLU: 2 KB into the chunk
+    const int sub0 = n0 / kSubRows;                 // first 16-row sub-tile of those columns
     const int nkb = p.K / kKBlock;
 
     if (tid == 0) {
@@ -252,19 +250,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const uint64_t stream_policy = ptx::policy_evict_first();
+            ptx::prefetch_tmap(&tmap_a);
+            ptx::prefetch_tmap(&tmap_w0);
+            if (SWIGLU) ptx::prefetch_tmap(&tmap_w1);
             int kb = 0;
             for (; kb < nkb; ++kb) {
                 const int s = kb % STAGES;
                 const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
                 if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err, p.wait_ns)) break;
-                const uint32_t wbytes = (uint32_t)R * 32u;  // this CTA's rows of one weight set
-                ptx::mbar_arrive_expect_tx(&full[s], (uint32_t)L.b_stage + (SWIGLU ? 2u : 1u) * wbytes);
+                // One box of COLS/16 sub-tiles x one k-block per weight set (sub-tiles
+                // past N read as zero), full size in bytes whatever the ragged edge.
+                ptx::mbar_arrive_expect_tx(&full[s], (uint32_t)L.b_stage + (uint32_t)kChunk);
                 ptx::tma_load_2d(smem + (size_t)s * L.b_stage, &tmap_a, kb * kKBlock, m0, &full[s]);
-                const size_t off = chunk_offset(nt0, p.N, p.K, kb) + half_off;
                 unsigned char *wdst = smem + L.w_off + (size_t)s * kChunk;
-                ptx::bulk_g2s_hint(wdst, p.w[0].q_rep + off, wbytes, &full[s], stream_policy);
+                ptx::tma_load_3d_hint(wdst, &tmap_w0, 0, kb, sub0, &full[s], stream_policy);
                 if (SWIGLU)  // up rows in the second half of the slot
-                    ptx::bulk_g2s_hint(wdst + kChunk / 2, p.w[1].q_rep + off, wbytes, &full[s], stream_policy);
+                    ptx::tma_load_3d_hint(wdst + kChunk / 2, &tmap_w1, 0, kb, sub0, &full[s], stream_policy);
             }
             if (*abort_flag) {  // let issued copies land before the CTA can exit
                 volatile int no_abort = 0;
@@ -458,48 +459,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-// TMA map over A [M][K] fp16: boxes of 64 k x T tokens, 128-byte swizzle, zero fill.
-bool make_tmap_a(CUtensorMap *map, const __half *A, int M, int K, int T) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kKBlock, (cuuint32_t)T};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(A), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 template <int GROUP, bool SWIGLU>
 cudaError_t launch_tc_one(const TcParams &p, int T, cudaStream_t s) {
     using Sh = TcShape;
-    CUtensorMap map;
-    if (!make_tmap_a(&map, p.A, p.M, p.K, T)) return cudaErrorInvalidValue;
+    const int cols = SWIGLU ? 64 : kTileRows;  // output columns per CTA
+    CUtensorMap map_a, map_w0, map_w1;
+    if (!tmap_activations(&map_a, p.A, p.M, p.K, T)) return cudaErrorInvalidValue;
+    if (!tmap_weights(&map_w0, p.w[0].q_rep, p.N, p.K, 1, cols / kSubRows)) return cudaErrorInvalidValue;
+    if (!tmap_weights(&map_w1, p.w[1].q_rep, p.N, p.K, 1, cols / kSubRows)) return cudaErrorInvalidValue;
     const TcSmem L = tc_smem(T, Sh::STAGES, Sh::ASTAGES, Sh::NS);
     // One CTA per SM: the kernel takes all 512 tensor-memory columns.
     const size_t smem = (L.total + 1024 > 120 * 1024) ? L.total + 1024 : 120 * 1024;
     auto kern = tc_kernel<GROUP, SWIGLU>;
     cudaError_t e = ensure_max_dyn_smem(reinterpret_cast<const void *>(kern), 227 * 1024);
     if (e != cudaSuccess) return e;
-    const int cols = SWIGLU ? 64 : kTileRows;  // output columns per CTA
     dim3 grid((unsigned)((p.M + T - 1) / T), (unsigned)((p.N + cols - 1) / cols), 1);
-    kern<<<grid, kThreads, smem, s>>>(map, p, T);
+    kern<<<grid, kThreads, smem, s>>>(map_a, map_w0, map_w1, p, T);
     return cudaGetLastError();
 }
 

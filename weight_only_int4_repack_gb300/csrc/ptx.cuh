@@ -70,6 +70,8 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // phase incomplete): records W4A16_ERR_TIMEOUT in *err, raises the CTA's abort
 // flag and returns false. Also returns false once another thread of the CTA has
 // raised the abort flag.
+// Polls with a suspend-time hint, so a waiting warp takes few issue slots from
+// the warps that have work (an unhinted poll loop measured slower).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                           unsigned int *err, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -123,6 +125,30 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, 
         "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+
+// 3-D tiled tensor copy global -> shared.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, int y, int z, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 3-D tiled tensor copy global -> shared with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(void *dst, const void *tmap, int x, int y, int z, uint64_t *bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// Bring a tensor map into the constant cache ahead of its first copy.
+__device__ __forceinline__ void prefetch_tmap(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {

@@ -1,4 +1,5 @@
-// Device repack of nibble-packed int4 weights into the fragment-interleaved layout.
+// Device repack of nibble-packed int4 weights into the fragment-interleaved layout
+// (16-row sub-tiles, each one contiguous run of 512-byte pieces along K).
 //
 // The MatMulNBits Marlin pull request (github.com/justinchuby/onnx-genai pull 960,
 // "What's landed") repacks the ONNX nibble format once, on the device, into a
@@ -16,19 +17,16 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
                                                      long long n_chunks) {
     long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= n_chunks) return;
-    const long long chunks_per_full_tile = (long long)kTileRows * K / 32;  // 16-byte chunks
-    const int T = (int)(c / chunks_per_full_tile);
-    const int n0 = T * kTileRows;
-    const int R = min(kTileRows, N - n0);
-    const long long off = c - (long long)T * chunks_per_full_tile;
-    const int b = (int)(off / (2 * R));
-    const int rem = (int)(off % (2 * R));
-    const int s = rem >> 5;
-    const int slot = rem & 31;
+    // 16-byte chunk c is lane slot c % 32 of piece c / 32 = (sub-tile S, k-block b).
+    const long long piece = c >> 5;
+    const int kblocks = K / kKBlock;
+    const int S = (int)(piece / kblocks);
+    const int b = (int)(piece % kblocks);
+    const int slot = (int)(c & 31);
     // Slot 4g + (t + g/2) % 4 holds the fragment owned by (g, t).
     const int g = slot >> 2, t = ((slot & 3) - (g >> 1)) & 3;
     const size_t row_bytes = (size_t)(K / 2);
-    const uint8_t *r0 = q + (size_t)(n0 + s * kSubRows + g) * row_bytes;
+    const uint8_t *r0 = q + (size_t)(S * kSubRows + g) * row_bytes;
     const uint8_t *r1 = r0 + 8 * row_bytes;
     uint32_t w[4];
 #pragma unroll

@@ -92,8 +92,7 @@ w4a16_status check_weights(const uint8_t *q_rep, const void *scales, w4a16_scale
 
 struct Plan {
     int path;
-    int split;
-    int kc;
+    SmallMPlan sm;  // small-M path only
 };
 
 // The tensor-core kernel costs nearly the same for any M up to its token tile,
@@ -114,7 +113,7 @@ bool tc_preferred(int M, int N, bool swiglu) {
     return 3 * ctas >= 2LL * sm_count();
 }
 
-w4a16_status make_plan(int M, int N, int K, int group, int split_k, bool swiglu, Plan *out) {
+w4a16_status make_plan(int M, int N, int K, int group, int split_k, bool swiglu, bool scale_f32, Plan *out) {
     if (split_k < 0 || split_k > 8) return W4A16_ERR_INVALID_ARG;
     Plan p{};
     const int smax = g_smallm_max;
@@ -122,14 +121,12 @@ w4a16_status make_plan(int M, int N, int K, int group, int split_k, bool swiglu,
     if (M <= smax && (split_k > 0 || !tc_preferred(M, N, swiglu))) {
         p.path = W4A16_PATH_SMALL_M;
         if (split_k > K / (group > kKBlock ? group : kKBlock)) return W4A16_ERR_UNSUPPORTED;
-        const SmallMPlan sp = smallm_plan(M, N, K, group, swiglu, split_k, sm_count());
-        if (sp.split <= 0) return W4A16_ERR_UNSUPPORTED;
-        p.split = sp.split;
-        p.kc = sp.kc;
+        (void)scale_f32;
+        p.sm = smallm_plan(M, N, K, group, swiglu, split_k, sm_count());
+        if (p.sm.split <= 0) return W4A16_ERR_UNSUPPORTED;
     } else {
         p.path = W4A16_PATH_TCGEN05;
-        p.split = 1;
-        p.kc = 0;
+        p.sm = SmallMPlan{1, 0, 0, 0};
     }
     *out = p;
     return W4A16_OK;
@@ -163,9 +160,74 @@ __global__ void silu_mul_kernel(const uint4 *__restrict__ G, const uint4 *__rest
     }
 }
 
+// ---------------------------------------------------------------------------
+// RMS-norm prologue: An[m,k] = fp16(A[m,k] * r_m * gamma[k]),
+// r_m = 1 / sqrt(mean_k A[m,k]^2 + eps), fp32 arithmetic. One CTA per row; the
+// sum of squares is reduced in a fixed order (deterministic).
+// ---------------------------------------------------------------------------
+constexpr int kNormThreads = 256;
+
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const uint4 *__restrict__ A, const uint4 *__restrict__ gamma,
+                                                               uint4 *__restrict__ An, int K, float eps) {
+    __shared__ float red[kNormThreads / 32];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // A may be the previous kernel's output
+    const int nv = K / 8;
+    const uint4 *row = A + (size_t)blockIdx.x * nv;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < nv; i += kNormThreads) {
+        const uint4 x = row[i];
+        const __half2 *h = reinterpret_cast<const __half2 *>(&x);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(h[e]);
+            ss = fmaf(f.x, f.x, ss);
+            ss = fmaf(f.y, f.y, ss);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
+    const float r = 1.0f / sqrtf(tot / (float)K + eps);
+    uint4 *out = An + (size_t)blockIdx.x * nv;
+    for (int i = threadIdx.x; i < nv; i += kNormThreads) {
+        const uint4 x = row[i], gv = gamma[i];
+        const __half2 *h = reinterpret_cast<const __half2 *>(&x);
+        const __half2 *gh = reinterpret_cast<const __half2 *>(&gv);
+        uint4 y;
+        __half2 *yh = reinterpret_cast<__half2 *>(&y);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(h[e]);
+            const float2 gf = __half22float2(gh[e]);
+            yh[e] = __floats2half2_rn(f.x * r * gf.x, f.y * r * gf.y);
+        }
+        out[i] = y;
+    }
+}
+
 }  // namespace
 
 namespace w4a16 {
+cudaError_t launch_rmsnorm(const __half *A, const __half *gamma, __half *An, int M, int K, float eps, bool overlap,
+                           cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)M, 1, 1);
+    cfg.blockDim = dim3(kNormThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, rmsnorm_kernel, reinterpret_cast<const uint4 *>(A),
+                              reinterpret_cast<const uint4 *>(gamma), reinterpret_cast<uint4 *>(An), K, eps);
+}
+
 cudaError_t launch_silu_mul(const __half *G, const __half *U, __half *Y, size_t n, cudaStream_t s) {
     const size_t n_vec = n / 8;  // n is a multiple of 8 (N % 16 == 0)
     const int threads = 256;
@@ -213,30 +275,29 @@ w4a16_status w4a16_unpack_host(const uint8_t *q_rep, uint8_t *q, int N, int K) {
     if (!q_rep || !q || N <= 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
     if (N % kSubRows || K % kKBlock) return W4A16_ERR_UNSUPPORTED;
     const size_t row_bytes = (size_t)K / 2;
-    for (int n0 = 0; n0 < N; n0 += kTileRows) {
-        const int R = (N - n0) < kTileRows ? (N - n0) : kTileRows;
-        for (int b = 0; b < K / kKBlock; ++b) {
-            const uint8_t *chunk = q_rep + chunk_offset(n0, N, K, b);
-            for (int s = 0; s < R / kSubRows; ++s)
-                for (int slot = 0; slot < 32; ++slot) {
-                    const int g = slot / 4, t = ((slot % 4) - g / 2 + 4) % 4;
-                    for (int j = 0; j < 4; ++j) {
-                        const uint8_t *wp = chunk + s * kSubBytes + slot * 16 + j * 4;
-                        const uint32_t word = (uint32_t)wp[0] | ((uint32_t)wp[1] << 8) |
-                                              ((uint32_t)wp[2] << 16) | ((uint32_t)wp[3] << 24);
-                        for (int h = 0; h < 2; ++h) {
-                            const int row = n0 + s * kSubRows + g + 8 * h;
-                            for (int e = 0; e < 4; ++e) {
-                                const int p = 4 * (e % 2) + 2 * (e / 2) + h;
-                                const uint8_t nib = (uint8_t)((word >> (4 * p)) & 0xF);
-                                const int k = b * kKBlock + 16 * j + 4 * t + e;
-                                uint8_t &dst = q[(size_t)row * row_bytes + k / 2];
-                                dst = (k % 2 == 0) ? (uint8_t)((dst & 0xF0) | nib)
-                                                   : (uint8_t)((dst & 0x0F) | (nib << 4));
-                            }
+    const int kblocks = K / kKBlock;
+    for (int S = 0; S < N / kSubRows; ++S) {
+        for (int b = 0; b < kblocks; ++b) {
+            const uint8_t *piece = q_rep + piece_offset(S, b, K);
+            for (int slot = 0; slot < 32; ++slot) {
+                const int g = slot / 4, t = ((slot % 4) - g / 2 + 4) % 4;
+                for (int j = 0; j < 4; ++j) {
+                    const uint8_t *wp = piece + slot * 16 + j * 4;
+                    const uint32_t word = (uint32_t)wp[0] | ((uint32_t)wp[1] << 8) |
+                                          ((uint32_t)wp[2] << 16) | ((uint32_t)wp[3] << 24);
+                    for (int h = 0; h < 2; ++h) {
+                        const int row = S * kSubRows + g + 8 * h;
+                        for (int e = 0; e < 4; ++e) {
+                            const int p = 4 * (e % 2) + 2 * (e / 2) + h;
+                            const uint8_t nib = (uint8_t)((word >> (4 * p)) & 0xF);
+                            const int k = b * kKBlock + 16 * j + 4 * t + e;
+                            uint8_t &dst = q[(size_t)row * row_bytes + k / 2];
+                            dst = (k % 2 == 0) ? (uint8_t)((dst & 0xF0) | nib)
+                                               : (uint8_t)((dst & 0x0F) | (nib << 4));
                         }
                     }
                 }
+            }
         }
     }
     return W4A16_OK;
@@ -251,10 +312,10 @@ w4a16_status w4a16_gemm_plan(int M, int N, int K, int group, int split_k, int *p
     w4a16_status st = check_shape(M, N, K, group);
     if (st != W4A16_OK) return st;
     Plan p;
-    st = make_plan(M, N, K, group, split_k, false, &p);
+    st = make_plan(M, N, K, group, split_k, false, false, &p);
     if (st != W4A16_OK) return st;
     if (path) *path = p.path;
-    if (split_out) *split_out = p.split;
+    if (split_out) *split_out = p.sm.split;
     return W4A16_OK;
 }
 
@@ -262,7 +323,7 @@ static w4a16_status gemm_impl(const uint16_t *A, const WeightSet *ws_sets, int n
                               w4a16_scale_dtype sdt, uint16_t *Y, int M, int N, int K, int group,
                               int split_k, cudaStream_t stream) {
     Plan plan;
-    w4a16_status st = make_plan(M, N, K, group, split_k, nsets == 2, &plan);
+    w4a16_status st = make_plan(M, N, K, group, split_k, nsets == 2, sdt == W4A16_SCALE_F32, &plan);
     if (st != W4A16_OK) return st;
     unsigned int *err = device_error_ptr();
     if (!err) return W4A16_ERR_CUDA;
@@ -285,8 +346,8 @@ static w4a16_status gemm_impl(const uint16_t *A, const WeightSet *ws_sets, int n
     p.Y = reinterpret_cast<__half *>(Y);
     p.M = M; p.N = N; p.K = K; p.G = K / group;
     p.scale_f32 = sdt == W4A16_SCALE_F32;
-    p.split = plan.split;
-    p.kc_blocks = plan.kc;
+    p.split = plan.sm.split;
+    p.kc_blocks = plan.sm.kc;
     p.overlap = g_launch_overlap;
     p.err = err;
     p.wait_ns = g_wait_ns;
@@ -333,7 +394,7 @@ w4a16_status w4a16_gemm_swiglu(const uint16_t *A,
     const size_t need = w4a16_swiglu_workspace_bytes(M, N, K, group, 0);
     if (!ws || ws_bytes < need || !aligned(ws, 256)) return W4A16_ERR_WORKSPACE;
     Plan plan;
-    if ((st = make_plan(M, N, K, group, 0, false, &plan)) != W4A16_OK) return st;
+    if ((st = make_plan(M, N, K, group, 0, false, sdt == W4A16_SCALE_F32, &plan)) != W4A16_OK) return st;
     uint16_t *Gb = reinterpret_cast<uint16_t *>(ws);
     uint16_t *Ub = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(ws) +
                                                  align_up((size_t)M * N * 2, 256));
@@ -342,6 +403,70 @@ w4a16_status w4a16_gemm_swiglu(const uint16_t *A,
     return from_cuda(launch_silu_mul(reinterpret_cast<const __half *>(Gb),
                                      reinterpret_cast<const __half *>(Ub),
                                      reinterpret_cast<__half *>(Y), (size_t)M * N, s));
+}
+
+size_t w4a16_rmsnorm_workspace_bytes(int M, int N, int K, int group, int mode) {
+    if (M <= 0 || N <= 0 || K <= 0 || mode < 0 || mode > 2) return 0;
+    const size_t norm = align_up((size_t)M * K * 2, 256);
+    return norm + (mode == 2 ? w4a16_swiglu_workspace_bytes(M, N, K, group, 0) : 0);
+}
+
+// Shared front half of the RMS-norm entry points: validates, stages the
+// normalised activations at the start of ws and returns them.
+static w4a16_status rmsnorm_prologue(const uint16_t *A, const uint16_t *gamma, float eps, int M, int N, int K,
+                                     int group, int mode, void *ws, size_t ws_bytes, cudaStream_t s,
+                                     uint16_t **An) {
+    w4a16_status st = check_shape(M, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (!A || !gamma || !aligned(A, 16) || !aligned(gamma, 16)) return W4A16_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || eps != eps) return W4A16_ERR_INVALID_ARG;
+    if (!ws || !aligned(ws, 256) || ws_bytes < w4a16_rmsnorm_workspace_bytes(M, N, K, group, mode))
+        return W4A16_ERR_WORKSPACE;
+    *An = reinterpret_cast<uint16_t *>(ws);
+    return W4A16_OK;
+}
+
+w4a16_status w4a16_gemm_rmsnorm(const uint16_t *A, const uint16_t *gamma, float eps, const uint8_t *q_rep,
+                                const void *scales, w4a16_scale_dtype sdt, const uint8_t *zp, uint16_t *Y,
+                                int M, int N, int K, int group, int split_k, void *ws, size_t ws_bytes,
+                                void *stream) {
+    cudaStream_t s = (cudaStream_t)stream;
+    uint16_t *An = nullptr;
+    w4a16_status st = rmsnorm_prologue(A, gamma, eps, M, N, K, group, 0, ws, ws_bytes, s, &An);
+    if (st != W4A16_OK) return st;
+    if (!Y || !aligned(Y, 16)) return W4A16_ERR_INVALID_ARG;
+    if ((st = check_weights(q_rep, scales, sdt)) != W4A16_OK) return st;
+    Plan plan;
+    if ((st = make_plan(M, N, K, group, split_k, false, sdt == W4A16_SCALE_F32, &plan)) != W4A16_OK) return st;
+    if (cudaError_t e = launch_rmsnorm(reinterpret_cast<const __half *>(A), reinterpret_cast<const __half *>(gamma),
+                                       reinterpret_cast<__half *>(An), M, K, eps, g_launch_overlap != 0, s))
+        return from_cuda(e);
+    const WeightSet w{q_rep, scales, zp};
+    return gemm_impl(An, &w, 1, sdt, Y, M, N, K, group, split_k, s);
+}
+
+w4a16_status w4a16_gemm_swiglu_rmsnorm(const uint16_t *A, const uint16_t *gamma, float eps,
+                                       const uint8_t *qg_rep, const void *sg, const uint8_t *zg,
+                                       const uint8_t *qu_rep, const void *su, const uint8_t *zu,
+                                       w4a16_scale_dtype sdt, uint16_t *Y, int M, int N, int K, int group,
+                                       int fused, void *ws, size_t ws_bytes, void *stream) {
+    cudaStream_t s = (cudaStream_t)stream;
+    uint16_t *An = nullptr;
+    const int mode = fused ? 1 : 2;
+    w4a16_status st = rmsnorm_prologue(A, gamma, eps, M, N, K, group, mode, ws, ws_bytes, s, &An);
+    if (st != W4A16_OK) return st;
+    if (!Y || !aligned(Y, 16)) return W4A16_ERR_INVALID_ARG;
+    if ((st = check_weights(qg_rep, sg, sdt)) != W4A16_OK) return st;
+    if ((st = check_weights(qu_rep, su, sdt)) != W4A16_OK) return st;
+    Plan plan;
+    if ((st = make_plan(M, N, K, group, 0, fused != 0, sdt == W4A16_SCALE_F32, &plan)) != W4A16_OK) return st;
+    if (cudaError_t e = launch_rmsnorm(reinterpret_cast<const __half *>(A), reinterpret_cast<const __half *>(gamma),
+                                       reinterpret_cast<__half *>(An), M, K, eps, g_launch_overlap != 0, s))
+        return from_cuda(e);
+    const size_t norm = align_up((size_t)M * K * 2, 256);
+    void *rest = reinterpret_cast<uint8_t *>(ws) + norm;
+    return w4a16_gemm_swiglu(An, qg_rep, sg, zg, qu_rep, su, zu, sdt, Y, M, N, K, group, fused, fused ? nullptr : rest,
+                             fused ? 0 : ws_bytes - norm, stream);
 }
 
 w4a16_status w4a16_set_tuning(int smallm_max) {

@@ -2,6 +2,7 @@
 // Not installed; the public interface is include/w4a16.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -16,10 +17,10 @@ constexpr int kSubRows = 16;     // rows per sub-tile (one warp's MMA row block)
 constexpr int kKBlock = 64;      // k per k-block
 constexpr int kSubBytes = 512;   // bytes of one 16-row x 64-k sub-tile
 
-// Byte offset of chunk (row tile starting at n0, k-block b).
-__host__ __device__ inline size_t chunk_offset(int n0, int N, int K, int b) {
-    int R = (N - n0) < kTileRows ? (N - n0) : kTileRows;
-    return (size_t)n0 * (size_t)(K / 2) + (size_t)b * (size_t)R * 32u;
+// Byte offset of piece (16-row sub-tile S, k-block b): every sub-tile is one
+// contiguous run of K/64 pieces of 512 bytes.
+__host__ __device__ inline size_t piece_offset(int S, int b, int K) {
+    return ((size_t)S * (size_t)(K / kKBlock) + (size_t)b) * (size_t)kSubBytes;
 }
 
 // ---------------------------------------------------------------------------
@@ -54,6 +55,29 @@ struct TcParams {
     unsigned long long wait_ns;  // limit of each bounded wait
 };
 
+// ---------------------------------------------------------------------------
+// Tensor maps (TMA descriptors), encoded once per buffer and shape and cached.
+// ---------------------------------------------------------------------------
+struct TmapDesc {
+    const void *ptr;
+    int dtype;               // CUtensorMapDataType
+    int rank;                // 2 or 3
+    uint64_t dims[3];        // elements, innermost first
+    uint64_t strides[2];     // bytes of dimensions 1 and 2
+    uint32_t box[3];
+    int swizzle128;          // 128-byte swizzle (else none)
+};
+bool encode_tmap(CUtensorMap *out, const TmapDesc &d);
+// Repacked weights as (512-byte piece, k-block, sub-tile): a box of
+// `kblocks_box` consecutive k-blocks of `subtiles_box` consecutive sub-tiles.
+bool tmap_weights(CUtensorMap *out, const uint8_t *q_rep, int N, int K, int kblocks_box, int subtiles_box);
+// Activations [M][K] fp16: boxes of 64 k x rows_box tokens, 128-byte swizzle,
+// tokens past M read as zero.
+bool tmap_activations(CUtensorMap *out, const __half *A, int M, int K, int rows_box);
+// The same activations as (64 k, token, k-block): one box brings `kblocks_box`
+// consecutive k-blocks of rows_box tokens, laid out k-block after k-block.
+bool tmap_activations_kblocks(CUtensorMap *out, const __half *A, int M, int K, int rows_box, int kblocks_box);
+
 // Number of SMs of the current device (cached per device, thread-safe).
 int sm_count();
 
@@ -63,9 +87,6 @@ cudaError_t ensure_max_dyn_smem(const void *func, int bytes);
 
 // Host-side launchers (return cudaError_t of the launch).
 cudaError_t launch_repack(const uint8_t *q, uint8_t *q_rep, int N, int K, cudaStream_t s);
-cudaError_t launch_smallm(const SmallMParams &p, int group, bool swiglu, cudaStream_t s);
-size_t smallm_smem_bytes(int M, int group, bool swiglu, int kc_blocks);
-int smallm_threads(int M, bool swiglu);
 
 struct SmallMPlan {
     int split;      // CTAs per row tile along K (cluster size, 1..8)
@@ -74,8 +95,11 @@ struct SmallMPlan {
     int per_sm;     // resident CTAs per SM at that shared-memory size
 };
 SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k, int sm_count);
+cudaError_t launch_smallm(const SmallMParams &p, int group, bool swiglu, cudaStream_t s);
 cudaError_t launch_tc(const TcParams &p, int group, bool swiglu, cudaStream_t s);
 int tc_tile_tokens(int M, bool swiglu);
+cudaError_t launch_rmsnorm(const __half *A, const __half *gamma, __half *An, int M, int K, float eps, bool overlap,
+                           cudaStream_t s);
 cudaError_t launch_silu_mul(const __half *G, const __half *U, __half *Y, size_t n,
                             cudaStream_t s);
 
