@@ -55,10 +55,11 @@ constexpr int kStages = 2;
 
 // Sub-tiles per consumer warp: two when the accumulators are small (shares the
 // activation fragments and the per-block overhead), else one.
+// A fused SwiGLU launch gives the gate and the up weight set CTAs of their own
+// (one cluster = the K ranks of both sets), so every CTA streams one set.
 template <int MT, bool SWIGLU>
 struct Shape {
-    static constexpr int NS = SWIGLU ? 2 : 1;
-    static constexpr int SUBT = (MT * NS <= 2) ? 2 : 1;
+    static constexpr int SUBT = (MT <= 2) ? 2 : 1;
     static constexpr int CW = 8 / SUBT;             // consumer warps
     static constexpr int THREADS = CW * 32 + 32;    // + one producer warp
     static constexpr int STAGES = kStages;
@@ -66,7 +67,7 @@ struct Shape {
     // grow, so that they stay in registers (measured at K=5120 N=13824: M=9
     // 16.4 vs 19.5 us, M=16 18.2 vs 20.3, M=32 32.6 vs 37.3 against the budget
     // of one token tile, which spilled).
-    static constexpr int MINB = MT * NS == 1 ? 4 : (MT * NS == 2 ? 3 : 1);
+    static constexpr int MINB = MT == 1 ? 4 : (MT == 2 ? 3 : 1);
 };
 
 // Compile-time loop: f(std::integral_constant<int, I>) for I in [B, E). Register
@@ -104,19 +105,18 @@ __device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)
 // the last 8-token tile read from.
 struct SmemPlan {
     int a_stride, ng;
-    size_t a_off, meta_off, meta_set_bytes, gsum_off, bar_off, total;
+    size_t a_off, meta_off, gsum_off, bar_off, total;
 };
 
-__host__ __device__ inline SmemPlan make_plan(int M, int MT, int group, int kc, int ns, int stages) {
+__host__ __device__ inline SmemPlan make_plan(int M, int MT, int group, int kc, int stages) {
     SmemPlan p;
-    p.a_off = (size_t)stages * ns * kStageSet;     // the weight ring comes first
+    p.a_off = (size_t)stages * kStageSet;          // the weight ring comes first
     p.a_stride = kc * kKBlock + 16;                 // +32 bytes per row: conflict-free fragment loads
     p.ng = (kc * kKBlock + group - 1) / group;      // groups of a chunk (chunks start on a group)
     p.meta_off = p.a_off + (size_t)(M + 1) * p.a_stride * 2;
-    p.meta_set_bytes = (size_t)kTileRows * p.ng * 8;  // float2 (s / f, (s / f)(1024 + f zp))
-    p.gsum_off = p.meta_off + ns * p.meta_set_bytes;  // float [ng][8 MT] group activation sums
-    const size_t main_end = p.gsum_off + (size_t)p.ng * 8 * MT * 4;
-    const size_t part_end = (size_t)ns * 8 * MT * kPartStride * 4;  // overlays the ring after use
+    p.gsum_off = p.meta_off + (size_t)kTileRows * p.ng * 8;  // meta: float2 (s / f, (s / f)(1024 + f zp))
+    const size_t main_end = p.gsum_off + (size_t)p.ng * 8 * MT * 4;  // float [ng][8 MT] group activation sums
+    const size_t part_end = (size_t)8 * MT * kPartStride * 4;  // overlays the ring after use
     const size_t end = main_end > part_end ? main_end : part_end;
     p.bar_off = (end + 15) / 16 * 16;
     p.total = p.bar_off + (size_t)(2 * stages + 2) * 8;  // full[], empty[], activation barrier, abort
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
     smallm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                   const SmallMParams p) {
     using Sh = Shape<MT, SWIGLU>;
-    constexpr int NS = Sh::NS, SUBT = Sh::SUBT, CW = Sh::CW, STAGES = Sh::STAGES;
+    constexpr int SUBT = Sh::SUBT, CW = Sh::CW, STAGES = Sh::STAGES;
     constexpr int NC = CW * 32;                            // consumer threads
     constexpr int SPG = GROUP / 16;                        // k16 steps per group
     constexpr int BPG = GROUP > kKBlock ? GROUP / kKBlock : 1;  // k-blocks per group (128: 2)
@@ -141,15 +141,18 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
     const int n0 = blockIdx.x * kTileRows;
     const int R = min(kTileRows, p.N - n0);
     const int nsub = R / kSubRows;
-    const int S = p.split;
-    const int rank = (S > 1) ? (int)ptx::cluster_rank() : 0;
+    const int S = p.split;                 // K ranks per weight set
+    const int CS = SWIGLU ? 2 * S : S;     // cluster size: the K ranks of the gate, then of the up set
+    const int crank = (CS > 1) ? (int)ptx::cluster_rank() : 0;
+    const int set = SWIGLU ? crank / S : 0;  // weight set this CTA streams (SwiGLU: 0 gate, 1 up)
+    const int rank = crank % S;
     // K ranges in whole groups, so that a group never straddles two ranks.
     const int nu = p.K / kKBlock / BPG;
     const int b_begin = (int)((long long)nu * rank / S) * BPG;
     const int b_end = (int)((long long)nu * (rank + 1) / S) * BPG;
     const int nstage = (b_end - b_begin + kBPS - 1) / kBPS;
     const int kc = p.kc_blocks;  // a multiple of kBPS unless it covers the whole range
-    const SmemPlan plan = make_plan(p.M, MT, GROUP, kc, NS, STAGES);
+    const SmemPlan plan = make_plan(p.M, MT, GROUP, kc, STAGES);
 
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + plan.bar_off);
     uint64_t *empty = full + STAGES;
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
     // Metadata of the first chunk, first batch of 8 groups per row: the loads are
     // issued before the barrier that releases the weight stream, so they are
     // ahead of it in the memory system (they are latency-critical, it is not).
-    constexpr int RPT = (NS * kTileRows + NC - 1) / NC;  // metadata rows per consumer thread
+    constexpr int RPT = (kTileRows + NC - 1) / NC;  // metadata rows per consumer thread
     const int zpstride = (p.G + 1) / 2;
     constexpr int PREB = RPT == 1 ? 2 : 1;  // prefetched batches of 8 groups
     float pre_s[RPT][PREB][8];
@@ -186,10 +189,12 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
     // groups outside [lo, hi) are not needed. fp16 scales in rows that start 16-byte
     // aligned (G % 8 == 0) come from one 16-byte load, their zero points from one
     // 4-byte load; other formats load each group.
-    auto load_meta_batch = [&](int row_set, int gbase, int lo, int hi, float (&sv)[8], uint32_t (&zb)[8]) {
-        const int w = row_set / kTileRows, row = row_set % kTileRows;
+    // Selected field by field: a runtime index into the parameter array would copy it to the stack.
+    const void *const set_scales = set ? p.w[1].scales : p.w[0].scales;
+    const uint8_t *const set_zp = set ? p.w[1].zp : p.w[0].zp;
+    auto load_meta_batch = [&](int row, int gbase, int lo, int hi, float (&sv)[8], uint32_t (&zb)[8]) {
         const int n = n0 + row;
-        const uint8_t *zrow = p.w[w].zp ? p.w[w].zp + (size_t)n * zpstride : nullptr;
+        const uint8_t *zrow = set_zp ? set_zp + (size_t)n * zpstride : nullptr;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             sv[u] = 0.f;
@@ -200,7 +205,7 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
         if (row >= R || gbase >= hi || gbase + 8 <= lo) return;
         if (!p.scale_f32 && (p.G & 7) == 0) {
             const uint4 x = __ldg(reinterpret_cast<const uint4 *>(
-                reinterpret_cast<const unsigned short *>(p.w[w].scales) + (size_t)n * p.G + gbase));
+                reinterpret_cast<const unsigned short *>(set_scales) + (size_t)n * p.G + gbase));
             const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
             const uint32_t zw = zrow ? __ldg(reinterpret_cast<const unsigned int *>(zrow + gbase / 2)) : 0x88888888u;
 #pragma unroll
@@ -214,8 +219,8 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                 const int grp = gbase + u;
                 if (grp >= lo && grp < hi) {
                     const size_t si = (size_t)n * p.G + grp;
-                    sv[u] = p.scale_f32 ? __ldg(reinterpret_cast<const float *>(p.w[w].scales) + si)
-                                        : __half2float(__ldg(reinterpret_cast<const __half *>(p.w[w].scales) + si));
+                    sv[u] = p.scale_f32 ? __ldg(reinterpret_cast<const float *>(set_scales) + si)
+                                        : __half2float(__ldg(reinterpret_cast<const __half *>(set_scales) + si));
                     if (zrow) zb[u] = __ldg(zrow + (grp >> 1));
                 }
             }
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
             const int rs = tid + NC * r;
-            if (rs < NS * kTileRows) {
+            if (rs < kTileRows) {
 #pragma unroll
                 for (int bt = 0; bt < PREB; ++bt)
                     load_meta_batch(rs, (grp_first0 & ~7) + 8 * bt, grp_first0, grp_first0 + ng_first0, pre_s[r][bt],
@@ -253,8 +258,8 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
             };
             if (pre == 0) start_activations();
             const uint64_t stream_policy = ptx::policy_evict_first();
-            ptx::prefetch_tmap(&tm_w0);
-            if (SWIGLU) ptx::prefetch_tmap(&tm_w1);
+            const CUtensorMap *tm_w = set ? &tm_w1 : &tm_w0;
+            ptx::prefetch_tmap(tm_w);
             int st = 0;
             for (; st < nstage; ++st) {
                 const int s = st % STAGES;
@@ -264,10 +269,9 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                 const int b0 = b_begin + st * kBPS;
                 // One box: kBPS k-blocks of the tile's eight sub-tiles (sub-tiles past N
                 // and k-blocks past K read as zero), [sub-tile][k-block][512 bytes].
-                ptx::mbar_arrive_expect_tx(&full[s], NS * kStageSet);
-                unsigned char *dst = smem + (size_t)s * NS * kStageSet;
-                ptx::tma_load_3d_hint(dst, &tm_w0, 0, b0, n0 / kSubRows, &full[s], stream_policy);
-                if (SWIGLU) ptx::tma_load_3d_hint(dst + kStageSet, &tm_w1, 0, b0, n0 / kSubRows, &full[s], stream_policy);
+                ptx::mbar_arrive_expect_tx(&full[s], kStageSet);
+                unsigned char *dst = smem + (size_t)s * kStageSet;
+                ptx::tma_load_3d_hint(dst, tm_w, 0, b0, n0 / kSubRows, &full[s], stream_policy);
             }
             if (!a_issued && !*abort_flag) start_activations();
             if (*abort_flag) {
@@ -294,7 +298,6 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) arow[mt] = min(8 * mt + g, p.M) * plan.a_stride;
         const float2 *meta0 = reinterpret_cast<const float2 *>(smem + plan.meta_off);
-        const int meta_set = (int)(plan.meta_set_bytes / 8);
         int mrow[SUBT][2];
 #pragma unroll
         for (int u = 0; u < SUBT; ++u) {
@@ -303,15 +306,13 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
             mrow[u][1] = (rg + 8) * plan.ng;
         }
 
-        float acc[NS][SUBT][MT][4];
+        float acc[SUBT][MT][4];
 #pragma unroll
-        for (int w = 0; w < NS; ++w)
+        for (int u = 0; u < SUBT; ++u)
 #pragma unroll
-            for (int u = 0; u < SUBT; ++u)
+            for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[w][u][mt][i] = 0.f;
+                for (int i = 0; i < 4; ++i) acc[u][mt][i] = 0.f;
 
         bool aborted = false;
         for (int c0 = b_begin; c0 < b_end; c0 += kc) {
@@ -328,11 +329,10 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
                 const int rs = tid + NC * r;
-                if (rs >= NS * kTileRows) continue;
-                const int w = rs / kTileRows, row = rs % kTileRows;
+                if (rs >= kTileRows) continue;
+                const int row = rs;
                 if (row >= R) continue;
-                float2 *meta = reinterpret_cast<float2 *>(smem + plan.meta_off + w * plan.meta_set_bytes) +
-                               (size_t)row * plan.ng;
+                float2 *meta = reinterpret_cast<float2 *>(smem + plan.meta_off) + (size_t)row * plan.ng;
                 const bool hi_row = (row >> 3) & 1;
                 const float f = hi_row ? 16.f : 1.f, inv_f = hi_row ? 0.0625f : 1.f;
                 const int gbase0 = grp0 & ~7;  // batches start on 8-group boundaries
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
             }
             ptx::named_bar_sync(1, NC);
 
-            float accg[NS][SUBT][MT][4];  // partial sum of the current group
+            float accg[SUBT][MT][4];  // partial sum of the current group
             const int st0 = (c0 - b_begin) / kBPS, st1 = (c1 - b_begin + kBPS - 1) / kBPS;
             for (int st = st0; st < st1; ++st) {
                 const int s = st % STAGES;
@@ -399,21 +399,17 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                 // Per-stage bases: every offset below them is a compile-time constant
                 // (weights sit in fixed 4 KB block slots, stages start on a group).
                 const unsigned char *wbase =
-                    smem + (size_t)s * NS * kStageSet + (warp * SUBT) * kSubStage + slot * 16;
+                    smem + (size_t)s * kStageSet + (warp * SUBT) * kSubStage + slot * 16;
                 const __half *abase = sA + (bs - c0) * kKBlock + 4 * t;
                 const float2 *mbase = meta0 + ((bs - c0) * kKBlock) / GROUP;
                 auto run_stage = [&](auto nbc) {
                     constexpr int NB = decltype(nbc)::value;
                     static_for<0, NB>([&](auto ic) {
                         constexpr int i = decltype(ic)::value;
-                        uint4 wv[NS][SUBT];
-                        static_for<0, NS>([&](auto wc) {
-                            constexpr int w = decltype(wc)::value;
-                            static_for<0, SUBT>([&](auto uc) {
-                                constexpr int u = decltype(uc)::value;
-                                wv[w][u] = *reinterpret_cast<const uint4 *>(wbase + w * kStageSet + u * kSubStage +
-                                                                           i * kSubBytes);
-                            });
+                        uint4 wv[SUBT];
+                        static_for<0, SUBT>([&](auto uc) {
+                            constexpr int u = decltype(uc)::value;
+                            wv[u] = *reinterpret_cast<const uint4 *>(wbase + u * kSubStage + i * kSubBytes);
                         });
                         static_for<0, 4>([&](auto jc) {
                             constexpr int j = decltype(jc)::value;
@@ -427,48 +423,41 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                                 bfr[mt][0] = v.x;
                                 bfr[mt][1] = v.y;
                             }
-                            static_for<0, NS>([&](auto wc) {
-                                constexpr int w = decltype(wc)::value;
-                                static_for<0, SUBT>([&](auto uc) {
-                                    constexpr int u = decltype(uc)::value;
-                                    const uint32_t word = j == 0 ? wv[w][u].x : j == 1 ? wv[w][u].y
-                                                        : j == 2 ? wv[w][u].z : wv[w][u].w;
-                                    const uint32_t w8 = word >> 8;
-                                    uint32_t a[4];
-                                    a[0] = lop_or<0x000F000Fu>(word);  // row g,   k 4t+0/1: 1024 + q
-                                    a[1] = lop_or<0x00F000F0u>(word);  // row g+8, k 4t+0/1: 1024 + 16 q
-                                    a[2] = lop_or<0x000F000Fu>(w8);    // row g,   k 4t+2/3
-                                    a[3] = lop_or<0x00F000F0u>(w8);    // row g+8, k 4t+2/3
+                            static_for<0, SUBT>([&](auto uc) {
+                                constexpr int u = decltype(uc)::value;
+                                const uint32_t word = j == 0 ? wv[u].x : j == 1 ? wv[u].y : j == 2 ? wv[u].z : wv[u].w;
+                                const uint32_t w8 = word >> 8;
+                                uint32_t a[4];
+                                a[0] = lop_or<0x000F000Fu>(word);  // row g,   k 4t+0/1: 1024 + q
+                                a[1] = lop_or<0x00F000F0u>(word);  // row g+8, k 4t+0/1: 1024 + 16 q
+                                a[2] = lop_or<0x000F000Fu>(w8);    // row g,   k 4t+2/3
+                                a[3] = lop_or<0x00F000F0u>(w8);    // row g+8, k 4t+2/3
 #pragma unroll
-                                    for (int mt = 0; mt < MT; ++mt) {
-                                        if constexpr (step % SPG == 0) {
-                                            const float z4[4] = {0.f, 0.f, 0.f, 0.f};
-                                            mma_16816(accg[w][u][mt], a, bfr[mt][0], bfr[mt][1], z4);
-                                        } else {
-                                            mma_16816(accg[w][u][mt], a, bfr[mt][0], bfr[mt][1], accg[w][u][mt]);
-                                        }
+                                for (int mt = 0; mt < MT; ++mt) {
+                                    if constexpr (step % SPG == 0) {
+                                        const float z4[4] = {0.f, 0.f, 0.f, 0.f};
+                                        mma_16816(accg[u][mt], a, bfr[mt][0], bfr[mt][1], z4);
+                                    } else {
+                                        mma_16816(accg[u][mt], a, bfr[mt][0], bfr[mt][1], accg[u][mt]);
                                     }
-                                });
+                                }
                             });
                             if constexpr (step % SPG == SPG - 1) {
                                 // Group complete: acc += (s / f) * acc_g.
                                 constexpr int gs = (i * kKBlock + 16 * j) / GROUP;  // group within the stage
-                                static_for<0, NS>([&](auto wc) {
-                                    constexpr int w = decltype(wc)::value;
-                                    static_for<0, SUBT>([&](auto uc) {
-                                        constexpr int u = decltype(uc)::value;
-                                        const float s0 = mbase[w * meta_set + mrow[u][0] + gs].x;
-                                        const float s1 = mbase[w * meta_set + mrow[u][1] + gs].x;
+                                static_for<0, SUBT>([&](auto uc) {
+                                    constexpr int u = decltype(uc)::value;
+                                    const float s0 = mbase[mrow[u][0] + gs].x;
+                                    const float s1 = mbase[mrow[u][1] + gs].x;
 #pragma unroll
-                                        for (int mt = 0; mt < MT; ++mt) {
-                                            float *ac = acc[w][u][mt];
-                                            const float *ag = accg[w][u][mt];
-                                            ac[0] = fmaf(s0, ag[0], ac[0]);
-                                            ac[1] = fmaf(s0, ag[1], ac[1]);
-                                            ac[2] = fmaf(s1, ag[2], ac[2]);
-                                            ac[3] = fmaf(s1, ag[3], ac[3]);
-                                        }
-                                    });
+                                    for (int mt = 0; mt < MT; ++mt) {
+                                        float *ac = acc[u][mt];
+                                        const float *ag = accg[u][mt];
+                                        ac[0] = fmaf(s0, ag[0], ac[0]);
+                                        ac[1] = fmaf(s0, ag[1], ac[1]);
+                                        ac[2] = fmaf(s1, ag[2], ac[2]);
+                                        ac[3] = fmaf(s1, ag[3], ac[3]);
+                                    }
                                 });
                             }
                         });
@@ -495,64 +484,60 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                     for (int mt = 0; mt < MT; ++mt) {
                         const float2 ag = *reinterpret_cast<const float2 *>(gsum + gi * 8 * MT + 8 * mt + 2 * t);
 #pragma unroll
-                        for (int w = 0; w < NS; ++w)
-#pragma unroll
-                            for (int u = 0; u < SUBT; ++u) {
-                                const float c0v = meta0[w * meta_set + mrow[u][0] + gi].y;
-                                const float c1v = meta0[w * meta_set + mrow[u][1] + gi].y;
-                                float *ac = acc[w][u][mt];
-                                ac[0] = fmaf(-c0v, ag.x, ac[0]);
-                                ac[1] = fmaf(-c0v, ag.y, ac[1]);
-                                ac[2] = fmaf(-c1v, ag.x, ac[2]);
-                                ac[3] = fmaf(-c1v, ag.y, ac[3]);
-                            }
+                        for (int u = 0; u < SUBT; ++u) {
+                            const float c0v = meta0[mrow[u][0] + gi].y;
+                            const float c1v = meta0[mrow[u][1] + gi].y;
+                            float *ac = acc[u][mt];
+                            ac[0] = fmaf(-c0v, ag.x, ac[0]);
+                            ac[1] = fmaf(-c0v, ag.y, ac[1]);
+                            ac[2] = fmaf(-c1v, ag.x, ac[2]);
+                            ac[3] = fmaf(-c1v, ag.y, ac[3]);
+                        }
                     }
                 }
             }
         }
 
-        // Partial tile -> shared memory as [set][token][row]; it overlays the ring,
+        // Partial tile -> shared memory as [token][row]; it overlays the ring,
         // which every consumer warp has finished with (all copies have landed).
         ptx::named_bar_sync(1, NC);
         float *P = reinterpret_cast<float *>(smem);
-        const size_t set_floats = (size_t)8 * MT * kPartStride;
 #pragma unroll
         for (int u = 0; u < SUBT; ++u) {
             if (!sub_ok[u]) continue;
             const int rg = (warp * SUBT + u) * kSubRows + g;
 #pragma unroll
-            for (int w = 0; w < NS; ++w)
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    float *Pw = P + w * set_floats;
-                    const int m0 = 8 * mt + 2 * t;
-                    Pw[(size_t)m0 * kPartStride + rg] = acc[w][u][mt][0];
-                    Pw[(size_t)(m0 + 1) * kPartStride + rg] = acc[w][u][mt][1];
-                    Pw[(size_t)m0 * kPartStride + rg + 8] = acc[w][u][mt][2];
-                    Pw[(size_t)(m0 + 1) * kPartStride + rg + 8] = acc[w][u][mt][3];
-                }
+            for (int mt = 0; mt < MT; ++mt) {
+                const int m0 = 8 * mt + 2 * t;
+                P[(size_t)m0 * kPartStride + rg] = acc[u][mt][0];
+                P[(size_t)(m0 + 1) * kPartStride + rg] = acc[u][mt][1];
+                P[(size_t)m0 * kPartStride + rg + 8] = acc[u][mt][2];
+                P[(size_t)(m0 + 1) * kPartStride + rg + 8] = acc[u][mt][3];
+            }
         }
     }
 
-    if (S > 1) ptx::cluster_sync(); else __syncthreads();
+    if (CS > 1) ptx::cluster_sync(); else __syncthreads();
     ptx::grid_dep_wait();  // Y may still be in use by the previous kernel
 
-    // Rank r finalises rows [r*R/S, (r+1)*R/S): partials of ranks 0..S-1 summed in order.
+    // Cluster rank r finalises rows [r*R/CS, (r+1)*R/CS): each set's partials of its
+    // K ranks summed in rank order, then (SwiGLU) silu(gate) * up.
     {
+        constexpr int NSET = SWIGLU ? 2 : 1;
         const float *P = reinterpret_cast<const float *>(smem);
-        const size_t set_floats = (size_t)8 * MT * kPartStride;
-        const int lo = (int)((long long)R * rank / S), hi = (int)((long long)R * (rank + 1) / S);
+        const int lo = (int)((long long)R * crank / CS), hi = (int)((long long)R * (crank + 1) / CS);
         const int nr = hi - lo;
         for (int i = tid; i < p.M * nr; i += Sh::THREADS) {
             const int m = i / nr, row = lo + i % nr;
-            float v[NS];
+            const float *src = P + (size_t)m * kPartStride + row;
+            float v[NSET];
 #pragma unroll
-            for (int w = 0; w < NS; ++w) {
-                const float *src = P + w * set_floats + (size_t)m * kPartStride + row;
-                if (S > 1) {
+            for (int w = 0; w < NSET; ++w) {
+                if (CS > 1) {
                     float part[8];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) part[q] = q < S ? ptx::ld_dsmem_f32(src, (uint32_t)q) : 0.f;
+                    for (int q = 0; q < 8; ++q)
+                        part[q] = q < S ? ptx::ld_dsmem_f32(src, (uint32_t)(w * S + q)) : 0.f;
                     float sum = part[0];
 #pragma unroll
                     for (int q = 1; q < 8; ++q)
@@ -563,11 +548,11 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                 }
             }
             float y = v[0];
-            if constexpr (SWIGLU) y = silu_f32(v[0]) * v[1];
+            if constexpr (SWIGLU) y = silu_f32(v[0]) * v[NSET - 1];
             p.Y[(size_t)m * p.N + n0 + row] = __float2half_rn(y);
         }
     }
-    if (S > 1) ptx::cluster_sync();  // keep shared memory alive until every peer has read it
+    if (CS > 1) ptx::cluster_sync();  // keep shared memory alive until every peer has read it
 }
 
 constexpr int kMaxDynSmem = 227 * 1024;
@@ -578,12 +563,12 @@ cudaError_t configure() {
     return ensure_max_dyn_smem(reinterpret_cast<const void *>(smallm_kernel<GROUP, MT, SWIGLU>), kMaxDynSmem);
 }
 
-// CTAs of a (1 x split) cluster launch that the device keeps resident at once.
+// CTAs of a (1 x cs) cluster launch that the device keeps resident at once.
 template <int GROUP, int MT, bool SWIGLU>
-int occupancy(size_t smem, int split) {
+int occupancy(size_t smem, int cs) {
     if (configure<GROUP, MT, SWIGLU>() != cudaSuccess) return 0;
     int n = 0;
-    if (split <= 1) {
+    if (cs <= 1) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, smallm_kernel<GROUP, MT, SWIGLU>,
                                                           Shape<MT, SWIGLU>::THREADS, smem) != cudaSuccess)
             return 0;
@@ -593,37 +578,38 @@ int occupancy(size_t smem, int split) {
         return n * sms;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1024, (unsigned)split, 1);
+    cfg.gridDim = dim3(1024, (unsigned)cs, 1);
     cfg.blockDim = dim3(Shape<MT, SWIGLU>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = (unsigned)split;
+    attr[0].val.clusterDim.y = (unsigned)cs;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaOccupancyMaxActiveClusters(&n, smallm_kernel<GROUP, MT, SWIGLU>, &cfg) != cudaSuccess) return 0;
-    return n * split;
+    return n * cs;
 }
 
 template <int GROUP, int MT, bool SWIGLU>
 cudaError_t launch_one(const SmallMParams &p, cudaStream_t s) {
-    const size_t smem = make_plan(p.M, MT, GROUP, p.kc_blocks, SWIGLU ? 2 : 1, Shape<MT, SWIGLU>::STAGES).total;
+    const size_t smem = make_plan(p.M, MT, GROUP, p.kc_blocks, Shape<MT, SWIGLU>::STAGES).total;
     auto kern = smallm_kernel<GROUP, MT, SWIGLU>;
     cudaError_t e = configure<GROUP, MT, SWIGLU>();
     if (e != cudaSuccess) return e;
+    const int cs = SWIGLU ? 2 * p.split : p.split;  // cluster: the K ranks of each weight set
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((p.N + kTileRows - 1) / kTileRows), (unsigned)p.split, 1);
+    cfg.gridDim = dim3((unsigned)((p.N + kTileRows - 1) / kTileRows), (unsigned)cs, 1);
     cfg.blockDim = dim3(Shape<MT, SWIGLU>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     int na = 0;
-    if (p.split > 1) {
+    if (cs > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
         attr[na].val.clusterDim.x = 1;
-        attr[na].val.clusterDim.y = (unsigned)p.split;
+        attr[na].val.clusterDim.y = (unsigned)cs;
         attr[na].val.clusterDim.z = 1;
         ++na;
     }
@@ -642,21 +628,21 @@ cudaError_t launch_one(const SmallMParams &p, cudaStream_t s) {
 }
 
 template <int GROUP, bool SWIGLU>
-int occupancy_mt(int M, size_t smem, int split) {
+int occupancy_mt(int M, size_t smem, int cs) {
     const int mt = (M + 7) / 8;
-    if (mt <= 1) return occupancy<GROUP, 1, SWIGLU>(smem, split);
-    if (mt <= 2) return occupancy<GROUP, 2, SWIGLU>(smem, split);
-    if (mt <= 4) return occupancy<GROUP, 4, SWIGLU>(smem, split);
-    return occupancy<GROUP, 8, SWIGLU>(smem, split);
+    if (mt <= 1) return occupancy<GROUP, 1, SWIGLU>(smem, cs);
+    if (mt <= 2) return occupancy<GROUP, 2, SWIGLU>(smem, cs);
+    if (mt <= 4) return occupancy<GROUP, 4, SWIGLU>(smem, cs);
+    return occupancy<GROUP, 8, SWIGLU>(smem, cs);
 }
 
 template <bool SWIGLU>
-int occupancy_group(int M, int group, size_t smem, int split) {
+int occupancy_group(int M, int group, size_t smem, int cs) {
     switch (group) {
-        case 16: return occupancy_mt<16, SWIGLU>(M, smem, split);
-        case 32: return occupancy_mt<32, SWIGLU>(M, smem, split);
-        case 64: return occupancy_mt<64, SWIGLU>(M, smem, split);
-        default: return occupancy_mt<128, SWIGLU>(M, smem, split);
+        case 16: return occupancy_mt<16, SWIGLU>(M, smem, cs);
+        case 32: return occupancy_mt<32, SWIGLU>(M, smem, cs);
+        case 64: return occupancy_mt<64, SWIGLU>(M, smem, cs);
+        default: return occupancy_mt<128, SWIGLU>(M, smem, cs);
     }
 }
 
@@ -685,16 +671,16 @@ int mt_of(int M) {
 }
 
 int threads_of(int M, bool swiglu) {
-    const int mt = mt_of(M);
-    const int ns = swiglu ? 2 : 1;
-    const int subt = (mt * ns <= 2) ? 2 : 1;
+    (void)swiglu;  // a SwiGLU CTA streams one weight set, as a plain one does
+    const int subt = (mt_of(M) <= 2) ? 2 : 1;
     return (8 / subt) * 32 + 32;
 }
 
 }  // namespace
 
 size_t smallm_smem_bytes(int M, int group, bool swiglu, int kc_blocks) {
-    return make_plan(M, mt_of(M), group, kc_blocks, swiglu ? 2 : 1, kStages).total;
+    (void)swiglu;
+    return make_plan(M, mt_of(M), group, kc_blocks, kStages).total;
 }
 
 int smallm_threads(int M, bool swiglu) { return threads_of(M, swiglu); }
@@ -705,7 +691,8 @@ int smallm_threads(int M, bool swiglu) { return threads_of(M, swiglu); }
 // on GB300 at M=8 K=5120 N=13824, split 4 (432 CTAs, at most 3 per SM) beats
 // split 5 (540 CTAs, up to 4 per SM) by 9%. Ties go to the larger grid (more
 // bytes in flight), then to fewer activation chunks. Without a one-wave plan,
-// concurrency per wave decides. A forced split only picks the chunk.
+// concurrency per wave decides. A forced split only picks the chunk. SwiGLU
+// launches a cluster of 2 x split CTAs (gate and up ranks), so split <= 4.
 SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k, int sm_count) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int, int, bool, int, int>, SmallMPlan> cache;
@@ -723,7 +710,7 @@ SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k,
     SmallMPlan best1{0, 0, 0, 0};
     long long best1_work = 0, best1_grid = 0;
     int best1_chunks = 0;
-    const int hi = split_k > 0 ? split_k : 8;
+    const int hi = split_k > 0 ? split_k : (swiglu ? 4 : 8);
     const int lo = split_k > 0 ? split_k : 1;
     for (int split = hi; split >= lo; --split) {
         if (split > nu) continue;
@@ -738,11 +725,13 @@ SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k,
             prev_kc = kc;
             const size_t smem = smallm_smem_bytes(M, group, swiglu, kc);
             if (smem > (size_t)kMaxDynSmem) continue;
-            const int resident = swiglu ? occupancy_group<true>(M, group, smem, split)
-                                        : occupancy_group<false>(M, group, smem, split);
+            const int cs = swiglu ? 2 * split : split;  // CTAs per cluster
+            if (cs > 8) continue;
+            const int resident = swiglu ? occupancy_group<true>(M, group, smem, cs)
+                                        : occupancy_group<false>(M, group, smem, cs);
             if (resident <= 0) continue;
             const int occ = (resident + sm_count - 1) / sm_count;
-            const long long grid = (long long)n_tiles * split;
+            const long long grid = (long long)n_tiles * cs;
             const long long slots = resident;
             const long long waves = (grid + slots - 1) / slots;
             if (waves == 1) {
