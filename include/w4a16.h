@@ -110,6 +110,22 @@ w4a16_status w4a16_gemm_plan(int M, int N, int K, int group, int split_k,
                              int *path, int *split_out);
 
 /*
+ * Launch shape of the kernel a call would run: w4a16_gemm (swiglu_fused = 0) or
+ * fused w4a16_gemm_swiglu (swiglu_fused = 1). For reports and tests; nothing is
+ * launched. `info` is a host pointer. Errors as w4a16_gemm_plan.
+ */
+typedef struct {
+    int path;          /* w4a16_path */
+    int split;         /* CTAs along K per weight set (1 on the tensor-core path) */
+    int ctas;          /* CTAs of the launch */
+    int threads;       /* threads per CTA */
+    int smem_bytes;    /* dynamic shared memory per CTA */
+    int stages;        /* shared-memory ring stages of the weight stream */
+} w4a16_launch_info;
+w4a16_status w4a16_gemm_launch_info(int M, int N, int K, int group, int split_k, int swiglu_fused,
+                                    w4a16_launch_info *info);
+
+/*
  * Y = A . dequant(q_rep)^T  (see the operation at the top of this file).
  *   A        device fp16 [M][K], 16-byte aligned
  *   q_rep    device, repacked weights from w4a16_repack (N x K)

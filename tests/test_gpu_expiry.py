@@ -49,13 +49,18 @@ def expire_then_recover(w4, call, ref):
     assert err <= 2e-2 * np.abs(ref).max(), err
 
 
-# Shapes whose CTAs stream more pipeline stages than their ring holds, so that
-# later stages are certainly still in flight when a consumer first polls them.
-@pytest.mark.parametrize("M,N,K,split", [(8, 13824, 5120, 0), (8, 4096, 14336, 1), (1, 4096, 28672, 8)])
+# Shapes whose CTAs stream more ring stages than their ring holds: the producer
+# reuses the first slot before the consumers can have released it (its data is
+# still in flight), so that wait is certainly incomplete when first tested.
+@pytest.mark.parametrize("M,N,K,split", [(8, 13824, 5120, 0), (8, 4096, 14336, 1), (1, 2048, 28672, 2),
+                                         (33, 4096, 14336, 2)])
 def test_small_m_wait_expiry(w4, M, N, K, split):
     c = make_case(M, N, K, 128, seed=70 + M)
     A, q, s, z = dev(c.A), w4.w4a16_repack(dev(c.bq)), dev(c.scales), dev(c.zp)
-    assert w4.w4a16_gemm_plan(M, N, K, 128, split)[0] == w4.W4A16_PATH_SMALL_M
+    info = w4.w4a16_gemm_launch_info(M, N, K, 128, split)
+    assert info["path"] == w4.W4A16_PATH_SMALL_M
+    stages_per_cta = -(-(K // 64 // info["split"]) // 4)
+    assert info["stages"] < stages_per_cta, info
     ref = oracle.gemm(c.A, c.bq, c.scales, c.zp, 128)
     expire_then_recover(w4, lambda: w4.w4a16_gemm(A, q, s, z, 128, split_k=split), ref)
 

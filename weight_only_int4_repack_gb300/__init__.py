@@ -44,10 +44,21 @@ EXPORTS = (
     "w4a16_swiglu_workspace_bytes", "w4a16_gemm_swiglu", "w4a16_set_tuning", "w4a16_set_launch_overlap",
     "w4a16_device_error", "w4a16_swiglu_static_scratch_bytes", "w4a16_gemm_swiglu_unfused_static",
     "w4a16_set_wait_limit_ns", "w4a16_rmsnorm_workspace_bytes", "w4a16_gemm_rmsnorm",
-    "w4a16_gemm_swiglu_rmsnorm",
+    "w4a16_gemm_swiglu_rmsnorm", "w4a16_gemm_launch_info",
 )
 
 _vp, _ci, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+
+class LaunchInfo(ctypes.Structure):
+    """w4a16_launch_info: launch shape of the kernel a call would run."""
+    _fields_ = [("path", _ci), ("split", _ci), ("ctas", _ci), ("threads", _ci), ("smem_bytes", _ci),
+                ("stages", _ci)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
 _sig = {
     "w4a16_status_string": (ctypes.c_char_p, [_ci]),
     "w4a16_repacked_bytes": (_sz, [_ci, _ci]),
@@ -55,6 +66,7 @@ _sig = {
     "w4a16_unpack_host": (_ci, [_vp, _vp, _ci, _ci]),
     "w4a16_gemm_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci]),
     "w4a16_gemm_plan": (_ci, [_ci, _ci, _ci, _ci, _ci, ctypes.POINTER(_ci), ctypes.POINTER(_ci)]),
+    "w4a16_gemm_launch_info": (_ci, [_ci, _ci, _ci, _ci, _ci, _ci, ctypes.POINTER(LaunchInfo)]),
     "w4a16_gemm": (_ci, [_vp, _vp, _vp, _ci, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _vp, _sz, _vp]),
     "w4a16_swiglu_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci]),
     "w4a16_gemm_swiglu": (_ci, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _vp,
@@ -138,6 +150,15 @@ def w4a16_gemm_plan(M, N, K, group, split_k=0) -> Tuple[int, int]:
     _check(lib.w4a16_gemm_plan(M, N, K, group, split_k, ctypes.byref(path), ctypes.byref(split)),
            "w4a16_gemm_plan")
     return path.value, split.value
+
+
+def w4a16_gemm_launch_info(M, N, K, group, split_k=0, swiglu_fused=False) -> dict:
+    """Launch shape of w4a16_gemm (or fused w4a16_gemm_swiglu): path, split, ctas,
+    threads, smem_bytes, stages."""
+    info = LaunchInfo()
+    _check(lib.w4a16_gemm_launch_info(M, N, K, group, split_k, int(bool(swiglu_fused)), ctypes.byref(info)),
+           "w4a16_gemm_launch_info")
+    return info.as_dict()
 
 
 def _scale_dtype(scales) -> int:

@@ -158,7 +158,13 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
     uint64_t *empty = full + STAGES;
     uint64_t *abar = empty + STAGES;  // activation chunk landed
     volatile int *abort_flag = reinterpret_cast<volatile int *>(abar + 1);
+    volatile int *a0_flag = abort_flag + 1;  // the producer issued the first activation chunk
     __half *sA = reinterpret_cast<__half *>(smem + plan.a_off);
+    // Activation chunks: the producer issues the first, consumer thread 0 each later
+    // one, only after it has seen the previous chunk land (one pending phase at
+    // most). Thread 0 counts the chunk phases it has seen and the last chunk it
+    // issued, so that after an abort it can wait for the one still in flight.
+    int a_seen = 0, a_last = -1;
 
     // Activations [M][c0*64, c1*64) of a chunk: one bulk copy per token row.
     auto issue_activations = [&](int c0, int c1) {
@@ -175,6 +181,7 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
         }
         ptx::mbar_init(abar, 1);
         *abort_flag = 0;
+        *a0_flag = 0;
         ptx::mbar_init_fence();
     }
     // Metadata of the first chunk, first batch of 8 groups per row: the loads are
@@ -253,6 +260,7 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
             bool a_issued = false;
             auto start_activations = [&]() {
                 ptx::grid_dep_wait();
+                *a0_flag = 1;
                 issue_activations(b_begin, min(b_begin + kc, b_end));
                 a_issued = true;
             };
@@ -281,7 +289,6 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                     const int last = s + ((st - 1 - s) / STAGES) * STAGES;
                     ptx::mbar_wait(&full[s], (uint32_t)(last / STAGES) & 1u, &no_abort, nullptr, 200000000ull);
                 }
-                if (a_issued) ptx::mbar_wait(abar, 0u, &no_abort, nullptr, 200000000ull);
             }
         }
         __syncwarp();
@@ -320,9 +327,12 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
             const int grp0 = (c0 * kKBlock) / GROUP;
             const int ng = ((c1 - c0) * kKBlock) / GROUP;
             ptx::named_bar_sync(1, NC);  // previous chunk consumed
-            if (tid == 0 && c0 != b_begin) {  // later chunks: generic reads of sA before the async writes
+            const int chunk_idx = (c0 - b_begin) / kc;
+            if (tid == 0 && c0 != b_begin && !aborted && !*abort_flag) {
+                // Generic reads of sA (previous chunk) before the async writes.
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 issue_activations(c0, c1);
+                a_last = chunk_idx;
             }
             // Per row and group: (s / f, (s / f)(1024 + f zp)), f = 16 for the second
             // row of each 16-row fragment block. One row per thread, loads batched.
@@ -360,8 +370,8 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                     }
                 }
             }
-            const int chunk_idx = (c0 - b_begin) / kc;
             if (!aborted && !ptx::mbar_wait(abar, (uint32_t)chunk_idx & 1u, abort_flag, p.err, p.wait_ns)) aborted = true;
+            if (!aborted) a_seen = chunk_idx + 1;
             // Group activation sums A_g[token] of this chunk (fp32 over the fp16
             // values), one (group, token) per thread with independent loads.
             {
@@ -518,6 +528,15 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
     }
 
     if (CS > 1) ptx::cluster_sync(); else __syncthreads();
+    if (tid == 0) {
+        // After an abort an activation chunk may still be in flight: the last one
+        // issued, if thread 0 has not seen it land. Wait (bounded) before exit.
+        const int last = a_last >= 0 ? a_last : (*a0_flag ? 0 : -1);
+        if (last >= a_seen) {
+            volatile int no_abort = 0;
+            ptx::mbar_wait(abar, (uint32_t)last & 1u, &no_abort, nullptr, 200000000ull);
+        }
+    }
     ptx::grid_dep_wait();  // Y may still be in use by the previous kernel
 
     // Cluster rank r finalises rows [r*R/CS, (r+1)*R/CS): each set's partials of its
@@ -705,9 +724,9 @@ SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k,
     const int bpg = group > kKBlock ? group / kKBlock : 1;  // k-blocks per group
     const int nu = K / kKBlock / bpg;                       // K split unit: whole groups
     const int n_tiles = (N + kTileRows - 1) / kTileRows;
-    SmallMPlan best{0, 0, 0, 0};
+    SmallMPlan best{};
     long long best_score = -1;              // multi-wave plans (used only if no one-wave plan)
-    SmallMPlan best1{0, 0, 0, 0};
+    SmallMPlan best1{};
     long long best1_work = 0, best1_grid = 0;
     int best1_chunks = 0;
     const int hi = split_k > 0 ? split_k : (swiglu ? 4 : 8);

@@ -498,6 +498,17 @@ int tc_tile_tokens(int M, bool swiglu) {
     return t < tmax ? t : tmax;
 }
 
+void tc_launch_shape(int M, int N, bool swiglu, int *ctas, int *threads, int *smem, int *stages) {
+    using Sh = TcShape;
+    const int T = tc_tile_tokens(M, swiglu);
+    const int cols = swiglu ? 64 : kTileRows;
+    const TcSmem L = tc_smem(T, Sh::STAGES, Sh::ASTAGES, Sh::NS);
+    *ctas = ((M + T - 1) / T) * ((N + cols - 1) / cols);
+    *threads = kThreads;
+    *smem = (int)((L.total + 1024 > 120 * 1024) ? L.total + 1024 : 120 * 1024);
+    *stages = Sh::STAGES;
+}
+
 cudaError_t launch_tc(const TcParams &p, int group, bool swiglu, cudaStream_t s) {
     const int T = tc_tile_tokens(p.M, swiglu);
     return swiglu ? launch_tc_group<true>(p, group, T, s) : launch_tc_group<false>(p, group, T, s);

@@ -36,6 +36,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  "r"(bytes)
                  : "memory");
 }
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Test of the phase that may block in hardware for a short, system-defined time.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -70,11 +83,14 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // phase incomplete): records W4A16_ERR_TIMEOUT in *err, raises the CTA's abort
 // flag and returns false. Also returns false once another thread of the CTA has
 // raised the abort flag.
-// Polls with a suspend-time hint, so a waiting warp takes few issue slots from
-// the warps that have work (an unhinted poll loop measured slower).
+// Later polls use a suspend-time hint, so a waiting warp takes few issue slots
+// from the warps that have work (an unhinted poll loop measured slower).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                           unsigned int *err, uint64_t limit_ns = kWaitLimitNs) {
-    if (mbar_try_wait(bar, parity)) return true;
+    // A zero limit (the test-only setting) must find an incomplete phase at once, so
+    // its first poll does not block; otherwise the first poll may block in hardware
+    // for a short, system-defined time.
+    if (limit_ns == 0 ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
 #pragma unroll 1
     for (uint32_t it = 0;; ++it) {

@@ -319,6 +319,30 @@ w4a16_status w4a16_gemm_plan(int M, int N, int K, int group, int split_k, int *p
     return W4A16_OK;
 }
 
+w4a16_status w4a16_gemm_launch_info(int M, int N, int K, int group, int split_k, int swiglu_fused,
+                                    w4a16_launch_info *info) {
+    w4a16_status st = check_shape(M, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (!info || (swiglu_fused != 0 && swiglu_fused != 1)) return W4A16_ERR_INVALID_ARG;
+    const bool sw = swiglu_fused == 1;
+    Plan p;
+    if ((st = make_plan(M, N, K, group, sw ? 0 : split_k, sw, false, &p)) != W4A16_OK) return st;
+    w4a16_launch_info r{};
+    r.path = p.path;
+    if (p.path == W4A16_PATH_TCGEN05) {
+        r.split = 1;
+        tc_launch_shape(M, N, sw, &r.ctas, &r.threads, &r.smem_bytes, &r.stages);
+    } else {  // small-M tile kernel
+        r.split = p.sm.split;
+        r.ctas = ((N + kTileRows - 1) / kTileRows) * p.sm.split * (sw ? 2 : 1);
+        r.threads = smallm_threads(M, sw);
+        r.smem_bytes = p.sm.smem;
+        r.stages = 2;
+    }
+    *info = r;
+    return W4A16_OK;
+}
+
 static w4a16_status gemm_impl(const uint16_t *A, const WeightSet *ws_sets, int nsets,
                               w4a16_scale_dtype sdt, uint16_t *Y, int M, int N, int K, int group,
                               int split_k, cudaStream_t stream) {

@@ -38,7 +38,7 @@ struct SmallMParams {
     __half *Y;              // [M][N]
     int M, N, K, G;
     int scale_f32;
-    int split;              // CTAs per row tile along K (cluster size)
+    int split;              // CTAs per row tile along K (cluster size; x2 for SwiGLU)
     int kc_blocks;          // k-blocks per staged activation chunk
     int overlap;            // launched as a programmatic dependent (weights read before the wait)
     unsigned int *err;      // device error word for bounded waits
@@ -98,6 +98,10 @@ SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k,
 cudaError_t launch_smallm(const SmallMParams &p, int group, bool swiglu, cudaStream_t s);
 cudaError_t launch_tc(const TcParams &p, int group, bool swiglu, cudaStream_t s);
 int tc_tile_tokens(int M, bool swiglu);
+// Launch shape of the tensor-core kernel: CTAs, threads, dynamic shared memory, ring stages.
+void tc_launch_shape(int M, int N, bool swiglu, int *ctas, int *threads, int *smem, int *stages);
+// Threads per CTA of the small-M tile kernel.
+int smallm_threads(int M, bool swiglu);
 cudaError_t launch_rmsnorm(const __half *A, const __half *gamma, __half *An, int M, int K, float eps, bool overlap,
                            cudaStream_t s);
 cudaError_t launch_silu_mul(const __half *G, const __half *U, __half *Y, size_t n,
