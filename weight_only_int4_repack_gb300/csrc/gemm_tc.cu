@@ -46,8 +46,6 @@ constexpr int kDqThreads = 128 * kDqParts;   // dequant / epilogue threads
 constexpr int kThreads = 64 + kDqThreads;    // warp 0 producer, warp 1 MMA + TMEM, then dequant/epilogue
 constexpr int kTmemCols = 512;
 constexpr int kChunk = kTileRows * 32;  // 4 KB weight chunk per 64-k block
-constexpr int kStageXS = kTileRows + 4;  // SwiGLU epilogue: floats per staged token row
-
 struct TcShape {
     static constexpr int NS = 1;        // one accumulator (SwiGLU pairs its rows inside it)
     static constexpr int TMAX = 256;    // tokens per tile (MMA N)
@@ -143,7 +141,10 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
     return r;
 }
 
-__device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
+// silu(x) = x / (1 + e^-x) with the hardware exponential and reciprocal intrinsics
+// (relative error about 1e-6, far below the fp16 rounding of the output): the
+// fused epilogue evaluates it for every output, unoverlapped with the MMAs.
+__device__ __forceinline__ float silu_f32(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 // Shared memory: [B stages (1024-aligned)] [W stages] [barriers] [tmem slot].
 struct TcSmem {
@@ -159,9 +160,6 @@ __host__ __device__ inline TcSmem tc_smem(int T, int stages, int astages, int ns
     p.b_stage = (size_t)T * 128;  // T token rows x 64 fp16
     p.w_off = p.b_stage * stages;
     p.bar_off = p.w_off + (size_t)stages * ns * kChunk;
-    // The SwiGLU epilogue stages its tokens over the ring: keep the barriers above it.
-    const size_t stage_end = (size_t)kDqParts * 16 * kStageXS * 4;
-    if (p.bar_off < stage_end) p.bar_off = stage_end;
     p.total = p.bar_off + (size_t)(2 * stages + 2 * astages + 2) * 8 + 16;
     return p;
 }
@@ -169,8 +167,8 @@ __host__ __device__ inline TcSmem tc_smem(int T, int stages, int astages, int ns
 // Per-row metadata of k-block kb for the k16 steps j0 .. j0+kSPW-1: half2
 // (1024 + zp) and half2 s (steps in one group share them).
 template <int GROUP>
-__device__ __forceinline__ void load_row_meta(const TcParams &p, int w, int n, int kb, int j0, uint32_t (&zz)[kSPW],
-                                              uint32_t (&ss)[kSPW]) {
+__device__ __forceinline__ void load_row_meta(const TcParams &p, const void *scales, const uint8_t *zp, int n, int kb,
+                                              int j0, uint32_t (&zz)[kSPW], uint32_t (&ss)[kSPW]) {
 #pragma unroll
     for (int jj = 0; jj < kSPW; ++jj) {
         if (jj > 0 && (16 * (j0 + jj)) / GROUP == (16 * (j0 + jj - 1)) / GROUP) {
@@ -181,11 +179,11 @@ __device__ __forceinline__ void load_row_meta(const TcParams &p, int w, int n, i
         const int grp = (kb * kKBlock + 16 * (j0 + jj)) / GROUP;
         const size_t si = (size_t)n * p.G + grp;
         float s;
-        if (p.scale_f32) s = __ldg(reinterpret_cast<const float *>(p.w[w].scales) + si);
-        else s = __half2float(__ldg(reinterpret_cast<const __half *>(p.w[w].scales) + si));
+        if (p.scale_f32) s = __ldg(reinterpret_cast<const float *>(scales) + si);
+        else s = __half2float(__ldg(reinterpret_cast<const __half *>(scales) + si));
         uint32_t z = 8;
-        if (p.w[w].zp) {
-            const uint8_t zb = __ldg(p.w[w].zp + (size_t)n * ((p.G + 1) / 2) + (grp >> 1));
+        if (zp) {
+            const uint8_t zb = __ldg(zp + (size_t)n * ((p.G + 1) / 2) + (grp >> 1));
             z = (grp & 1) ? (zb >> 4) : (zb & 0xFu);
         }
         const uint32_t zh = 0x6400u + z;  // fp16 bits of 1024 + zp
@@ -314,8 +312,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;              // tensor-memory lane quarter of this warp
         const int hf = (warp - 2) >> 2;      // which k16 steps (and which epilogue column chunks)
         const int r = q * 32 + lane;         // MMA row (= tensor-memory lane)
-        const int wset = SWIGLU ? r / COLS : 0;  // SwiGLU: rows 0-63 gate, 64-127 up
-        const int rr = r % COLS;             // output column within the CTA
+        // SwiGLU interleaves the sets by 16 rows: in each lane quarter, lanes 0-15 hold
+        // the gate rows and lanes 16-31 the up rows of the same 16 output columns, so
+        // the epilogue pairs them with one shuffle.
+        const int wset = SWIGLU ? (r >> 4) & 1 : 0;
+        const int rr = SWIGLU ? (r >> 5) * 16 + (r & 15) : r;  // output column within the CTA
+        // The row's weight set, selected field by field (a run-time index into the
+        // parameter array would copy it to the stack).
+        const void *const w_scales = wset ? p.w[1].scales : p.w[0].scales;
+        const uint8_t *const w_zp = wset ? p.w[1].zp : p.w[0].zp;
         const int n = n0 + rr;
         const bool row_ok = rr < R;
         const int sub = rr >> 4, g = r & 7, h = (r >> 3) & 1;
@@ -325,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t zz[NS][kSPW], ss[NS][kSPW];
         if (row_ok) {
 #pragma unroll
-            for (int w = 0; w < NS; ++w) load_row_meta<GROUP>(p, wset + w, n, 0, j0, zz[w], ss[w]);
+            for (int w = 0; w < NS; ++w) load_row_meta<GROUP>(p, w_scales, w_zp, n, 0, j0, zz[w], ss[w]);
         }
         bool aborted = false;
         for (int kb = 0; kb < nkb; ++kb) {
@@ -348,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ssn[w][jj] = ss[w][jj];
                         }
                     } else {
-                        load_row_meta<GROUP>(p, wset + w, n, kb + 1, j0, zzn[w], ssn[w]);
+                        load_row_meta<GROUP>(p, w_scales, w_zp, n, kb + 1, j0, zzn[w], ssn[w]);
                     }
                 }
             }
@@ -418,35 +423,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else {
-            // Each group of epilogue warps (one per lane quarter) stages 16 tokens
-            // x 128 rows in shared memory (the ring is idle once the last MMA has
-            // committed), then pairs gate row j with up row 64 + j.
-            // Every thread of the group runs the loop the same number of times,
-            // so the group barriers stay matched even after an abort.
-            constexpr int XS = kStageXS;      // floats per staged token row
-            float *xb = reinterpret_cast<float *>(smem) + (size_t)hf * 16 * XS;
-            const int gt = (warp - 2 - 4 * hf) * 32 + lane;  // thread in the group, 0..127
-            if (acc_ok) tc_fence_after();
-            for (int c0 = 16 * hf; c0 < T; c0 += 16 * kDqParts) {
-                uint32_t v[16];
-                tmem_ld16(tmem + lane_base + acc_col + (uint32_t)c0, v);
-                tmem_wait_ld();
+            // Lane r holds the gate (lanes 0-15 of a quarter) or the up (16-31) row of
+            // output column n: exchange half of each 16-token chunk with lane r ^ 16,
+            // then the gate lane finishes tokens 0-7 and the up lane tokens 8-15.
+            if (acc_ok) {
+                tc_fence_after();
+                const bool gate_lane = (lane & 16) == 0;
+                for (int c0 = 16 * hf; c0 < T; c0 += 16 * kDqParts) {
+                    uint32_t v[16];
+                    tmem_ld16(tmem + lane_base + acc_col + (uint32_t)c0, v);
+                    tmem_wait_ld();
+                    const int mb = m0 + c0 + (gate_lane ? 0 : 8);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) xb[i * XS + r] = __uint_as_float(v[i]);
-                ptx::named_bar_sync(1 + hf, 128);
-                if (acc_ok) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int idx = gt + 128 * k;
-                        const int i = idx / COLS, j = idx % COLS;
-                        const int m = m0 + c0 + i;
-                        if (m < p.M && j < R) {
-                            const float gv = xb[i * XS + j], uv = xb[i * XS + COLS + j];
-                            p.Y[(size_t)m * p.N + n0 + j] = __float2half_rn(silu_f32(gv) * uv);
-                        }
+                    for (int i = 0; i < 8; ++i) {
+                        const float own = __uint_as_float(gate_lane ? v[i] : v[8 + i]);
+                        const float peer = __shfl_xor_sync(0xffffffffu, __uint_as_float(gate_lane ? v[8 + i] : v[i]), 16);
+                        const float gv = gate_lane ? own : peer, uv = gate_lane ? peer : own;
+                        const int m = mb + i;
+                        if (row_ok && m < p.M) p.Y[(size_t)m * p.N + n] = __float2half_rn(silu_f32(gv) * uv);
                     }
                 }
-                ptx::named_bar_sync(1 + hf, 128);  // the buffer is rewritten next chunk
             }
         }
     }
