@@ -101,7 +101,7 @@ size_t w4a16_gemm_workspace_bytes(int M, int N, int K, int group, int split_k);
  * Which path and split factor w4a16_gemm would use. split_k as in w4a16_gemm.
  * path / split_out are host pointers (either may be NULL).
  * Path choice: M above the small-M limit (w4a16_set_tuning, default 64) takes
- * the tensor-core path; so does M >= 40 (33 for fused SwiGLU) when that path's
+ * the tensor-core path; so does M >= 33 (plain and fused SwiGLU) when that path's
  * grid (N/128 tiles, or N/64 for SwiGLU, times the token tiles) covers at least
  * two thirds of the SMs, unless split_k > 0 forces the small-M path's K split.
  * (This function reports the plain GEMM's choice.)

@@ -61,7 +61,8 @@ def test_path_choice(gpu_lib):
     small, tc = gpu_lib.W4A16_PATH_SMALL_M, gpu_lib.W4A16_PATH_TCGEN05
     assert gpu_lib.w4a16_gemm_plan(8, 13824, 5120, 128)[0] == small
     assert gpu_lib.w4a16_gemm_plan(32, 13824, 5120, 128)[0] == small
-    # From 40 tokens on, a grid of 108 tiles makes the tensor-core kernel faster ...
+    assert gpu_lib.w4a16_gemm_plan(33, 13824, 5120, 128)[0] == tc
+    # From 33 tokens on, a grid of 108 tiles makes the tensor-core kernel faster ...
     assert gpu_lib.w4a16_gemm_plan(48, 13824, 5120, 128)[0] == tc
     # ... but not one of 32 tiles, and a forced K split keeps the small-M path.
     assert gpu_lib.w4a16_gemm_plan(48, 4096, 4096, 128)[0] == small

@@ -709,9 +709,15 @@ int smallm_threads(int M, bool swiglu) { return threads_of(M, swiglu); }
 // the busiest SM streams (CTAs per SM, rounded up, x blocks per CTA): measured
 // on GB300 at M=8 K=5120 N=13824, split 4 (432 CTAs, at most 3 per SM) beats
 // split 5 (540 CTAs, up to 4 per SM) by 9%. Ties go to the larger grid (more
-// bytes in flight), then to fewer activation chunks. Without a one-wave plan,
-// concurrency per wave decides. A forced split only picks the chunk. SwiGLU
-// launches a cluster of 2 x split CTAs (gate and up ranks), so split <= 4.
+// bytes in flight), then to fewer activation chunks. Without a one-wave plan, a
+// time model decides: waves x (blocks an SM streams per wave + a fixed cost per
+// CTA). A forced split only picks the chunk. SwiGLU launches a cluster of
+// 2 x split CTAs (gate and up ranks), so split <= 4.
+// The fixed cost of one CTA (start, metadata, split-K reduction) in k-blocks of
+// streaming. At M=32 K=5120 N=13824 fused SwiGLU (CTAs of one per SM) it makes
+// split 2 (three waves of half ranges) win over split 1 (two waves of full ranges).
+constexpr int kFixedBlocks = 5;
+
 SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k, int sm_count) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int, int, bool, int, int>, SmallMPlan> cache;
@@ -725,7 +731,7 @@ SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k,
     const int nu = K / kKBlock / bpg;                       // K split unit: whole groups
     const int n_tiles = (N + kTileRows - 1) / kTileRows;
     SmallMPlan best{};
-    long long best_score = -1;              // multi-wave plans (used only if no one-wave plan)
+    long long best_score = -1;              // multi-wave plans (used only if no one-wave plan): cost
     SmallMPlan best1{};
     long long best1_work = 0, best1_grid = 0;
     int best1_chunks = 0;
@@ -766,10 +772,13 @@ SmallMPlan smallm_plan(int M, int N, int K, int group, bool swiglu, int split_k,
                 }
                 break;  // more chunks only shrink the chunk further
             }
-            // Concurrency per wave, discounted for extra waves and extra chunks.
-            const long long score = (grid / waves) * 64 / waves - (chunks - 1) * 2;
-            if (score > best_score) {
-                best_score = score;
+            // Time model in k-blocks: every wave streams its CTAs' ranges (the
+            // CTAs sharing an SM share its stream) plus a fixed start and
+            // reduction cost per CTA; extra activation chunks cost a little more.
+            const long long per_sm = (slots + sm_count - 1) / sm_count;
+            const long long cost = waves * (per_sm * per_rank + kFixedBlocks) + (chunks - 1) * 2;
+            if (best_score < 0 || cost < best_score) {
+                best_score = cost;
                 best = SmallMPlan{split, (int)kc, (int)smem, occ};
             }
         }

@@ -97,13 +97,14 @@ struct Plan {
 
 // The tensor-core kernel costs nearly the same for any M up to its token tile,
 // so from a few dozen tokens on it beats the stream kernel once its grid fills
-// most SMs. Measured on GB300 (us per call, stream kernel vs tensor-core
-// kernel): K=5120 N=13824 (108 tiles) M=32 37.5 vs 38.2, M=40 49.3 vs 38.5,
-// M=64 56.2 vs 38.6; K=N=4096 (32 tiles) M=64 15.8 vs 31.6.
-// Fused SwiGLU switches at 33 tokens, where the small-M kernel would need four
-// 8-token tiles for two weight sets (K=5120 N=13824, us per call: M=24 48.9 vs
-// 75.3, M=33 126.9 vs 76.1).
-constexpr int kTcMinM = 40;
+// most SMs. Past 32 tokens the stream kernel works on eight 8-token tiles (its
+// cost jumps), so both the plain GEMM and fused SwiGLU switch at 33 tokens.
+// Measured on GB300 (us per call, stream kernel vs tensor-core kernel): K=5120
+// N=13824 (108 tiles) M=32 29.2 vs 37.1, M=33 about 51 vs 37, M=40 49.3 vs 38.5,
+// M=64 56.2 vs 38.6; K=N=4096 (32 tiles, too few for the tensor-core grid)
+// M=64 15.8 vs 31.6. Fused SwiGLU at K=5120 N=13824: M=32 52.3 (stream, split 2)
+// vs 73 (tensor core), M=33 126.9 vs 73.0.
+constexpr int kTcMinM = 33;
 constexpr int kTcMinMSwiglu = 33;
 bool tc_preferred(int M, int N, bool swiglu) {
     if (M < (swiglu ? kTcMinMSwiglu : kTcMinM)) return false;
