@@ -40,8 +40,13 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kSPW = 2;                      // k16 steps of a block that one dequant warp converts (2 measured faster than 1)
-constexpr int kDqParts = 4 / kSPW;           // dequant warps per tensor-memory lane quarter
+// Dequantisation: kDqParts warp groups (one warp per tensor-memory lane quarter
+// each) take every kDqParts-th k-block, a thread converting all four k16 steps of
+// its row, so that more warps hide each other's latencies. Both ring depths are
+// multiples of kDqParts: then a group's next block in a ring slot is the slot's
+// very next use, so its parity wait can never match a phase two uses old.
+constexpr int kSPW = 4;                      // k16 steps of a block that one dequant thread converts
+constexpr int kDqParts = 3;                  // dequant warp groups (= warps per lane quarter)
 constexpr int kDqThreads = 128 * kDqParts;   // dequant / epilogue threads
 constexpr int kThreads = 64 + kDqThreads;    // warp 0 producer, warp 1 MMA + TMEM, then dequant/epilogue
 constexpr int kTmemCols = 512;
@@ -51,6 +56,7 @@ struct TcShape {
     static constexpr int TMAX = 256;    // tokens per tile (MMA N)
     static constexpr int STAGES = 6;    // shared-memory ring (TMA in flight)
     static constexpr int ASTAGES = 6;   // tensor-memory A stages: T + ASTAGES*32 <= 512
+    static_assert(STAGES % kDqParts == 0 && ASTAGES % kDqParts == 0, "ring depths: multiples of the dequant groups");
 };
 
 // ------------------------------------------------------------------ tcgen05
@@ -95,10 +101,21 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
                  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                  : "memory");
 }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
 template <int N>
 __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
-    static_assert(N == 8 || N == 16, "8 or 16 columns");
-    if constexpr (N == 16) tmem_st16(taddr, r);
+    static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
+    if constexpr (N == 32) tmem_st32(taddr, r);
+    else if constexpr (N == 16) tmem_st16(taddr, r);
     else tmem_st8(taddr, r);
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -227,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&empty[s], 1);
         }
         for (int s = 0; s < ASTAGES; ++s) {
-            ptx::mbar_init(&afull[s], kDqThreads);
+            ptx::mbar_init(&afull[s], kDqThreads / kDqParts);  // one warp group per block
             ptx::mbar_init(&aempty[s], 1);
         }
         ptx::mbar_init(accfull, 1);
@@ -310,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ dequant, then epilogue
         const int q = warp & 3;              // tensor-memory lane quarter of this warp
-        const int hf = (warp - 2) >> 2;      // which k16 steps (and which epilogue column chunks)
+        const int hf = (warp - 2) >> 2;      // warp group: k-blocks kb = hf (mod kDqParts), epilogue column chunks
         const int r = q * 32 + lane;         // MMA row (= tensor-memory lane)
         // SwiGLU interleaves the sets by 16 rows: in each lane quarter, lanes 0-15 hold
         // the gate rows and lanes 16-31 the up rows of the same 16 output columns, so
@@ -326,24 +343,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sub = rr >> 4, g = r & 7, h = (r >> 3) & 1;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int sh0 = 4 * h, sh1 = 4 * h + 8;  // nibble pairs (e0,e1) and (e2,e3) of this row
-        const int j0 = kSPW * hf;                // k16 steps j0 .. j0+kSPW-1 of every block
+        constexpr int j0 = 0;                    // all k16 steps of the group's blocks
         uint32_t zz[NS][kSPW], ss[NS][kSPW];
-        if (row_ok) {
+        if (row_ok && hf < nkb) {
 #pragma unroll
-            for (int w = 0; w < NS; ++w) load_row_meta<GROUP>(p, w_scales, w_zp, n, 0, j0, zz[w], ss[w]);
+            for (int w = 0; w < NS; ++w) load_row_meta<GROUP>(p, w_scales, w_zp, n, hf, j0, zz[w], ss[w]);
         }
         bool aborted = false;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = hf; kb < nkb; kb += kDqParts) {
             const int s = kb % STAGES, sa = kb % ASTAGES;
             const uint32_t ph = (uint32_t)(kb / STAGES) & 1u, pa = (uint32_t)(kb / ASTAGES) & 1u;
             if (!aborted && !ptx::mbar_wait(&full[s], ph, abort_flag, p.err, p.wait_ns)) aborted = true;
             if (!aborted && !ptx::mbar_wait(&aempty[sa], pa ^ 1u, abort_flag, p.err, p.wait_ns)) aborted = true;
             if (aborted) break;
-            // Next block's metadata, loaded early (it is used one block later).
+            // The group's next block's metadata, loaded early (it is used one block later).
+            const int kbn = kb + kDqParts;
             uint32_t zzn[NS][kSPW], ssn[NS][kSPW];
-            if (row_ok && kb + 1 < nkb) {
-                // With 128-wide groups, every other block continues the same group.
-                const bool same_group = GROUP > kKBlock && ((kb + 1) * kKBlock) / GROUP == (kb * kKBlock) / GROUP;
+            if (row_ok && kbn < nkb) {
+                const bool same_group = (kbn * kKBlock) / GROUP == (kb * kKBlock) / GROUP;
 #pragma unroll
                 for (int w = 0; w < NS; ++w) {
                     if (same_group) {
@@ -353,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ssn[w][jj] = ss[w][jj];
                         }
                     } else {
-                        load_row_meta<GROUP>(p, w_scales, w_zp, n, kb + 1, j0, zzn[w], ssn[w]);
+                        load_row_meta<GROUP>(p, w_scales, w_zp, n, kbn, j0, zzn[w], ssn[w]);
                     }
                 }
             }
@@ -365,16 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  wset * (kChunk / 2) + sub * kSubBytes;
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        // Words j0 .. j0+kSPW-1 of the row's lane slot for fragment column t.
-                        const unsigned char *slotp = chunk + (4 * g + ((t + (g >> 1)) & 3)) * 16 + 4 * j0;
-                        uint32_t words[kSPW];
-                        if constexpr (kSPW == 2) {
-                            const uint2 v = *reinterpret_cast<const uint2 *>(slotp);
-                            words[0] = v.x;
-                            words[kSPW - 1] = v.y;
-                        } else {
-                            words[0] = *reinterpret_cast<const uint32_t *>(slotp);
-                        }
+                        // The four words (k16 steps 0..3) of the row's lane slot for fragment column t.
+                        const unsigned char *slotp = chunk + (4 * g + ((t + (g >> 1)) & 3)) * 16;
+                        const uint4 v = *reinterpret_cast<const uint4 *>(slotp);
+                        const uint32_t words[kSPW] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                         for (int jj = 0; jj < kSPW; ++jj) {
                             const uint32_t lo = ((words[jj] >> sh0) & 0x000F000Fu) | 0x64006400u;  // k +0/1
@@ -387,13 +398,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 8 * kSPW; ++c) col[c] = 0u;
                 }
-                const uint32_t ta = tmem + lane_base + a_col0 + (uint32_t)((sa * NS + w) * 32 + 8 * kSPW * hf);
+                const uint32_t ta = tmem + lane_base + a_col0 + (uint32_t)((sa * NS + w) * 32);
                 tmem_st_cols(ta, col);
             }
             tmem_wait_st();
             tc_fence_before();
             ptx::mbar_arrive(&afull[sa]);
-            if (kb + 1 < nkb) {
+            if (kbn < nkb) {
 #pragma unroll
                 for (int w = 0; w < NS; ++w)
 #pragma unroll
