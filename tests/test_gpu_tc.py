@@ -132,3 +132,26 @@ def test_swiglu_forced_tc(tc_only, M, N, group):
 def test_no_device_error_recorded(gpu_lib):
     torch.cuda.synchronize()
     assert gpu_lib.w4a16_device_error() == gpu_lib.W4A16_OK
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (8, 13824, 5120), (32, 13824, 5120), (33, 13824, 5120),
+                                   (300, 1024, 2048), (1024, 13824, 5120)])
+def test_launch_info_matches_plan(gpu_lib, M, N, K):
+    # The launch-shape query reports the plan w4a16_gemm_plan reports, and a grid
+    # that covers the output: tiles of 128 columns (64 for fused SwiGLU on the
+    # tensor-core path) times the K split (x2 for SwiGLU on the small-M path).
+    path, split = gpu_lib.w4a16_gemm_plan(M, N, K, 128)
+    info = gpu_lib.w4a16_gemm_launch_info(M, N, K, 128)
+    assert (info["path"], info["split"]) == (path, split)
+    assert info["threads"] % 32 == 0 and 0 < info["smem_bytes"] <= 227 * 1024 + 1024
+    assert info["stages"] >= 2
+    if path == gpu_lib.W4A16_PATH_SMALL_M:
+        assert info["ctas"] == -(-N // 128) * split
+    else:
+        T = min(256, -(-M // 16) * 16)
+        assert info["ctas"] == -(-M // T) * -(-N // 128)
+    fused = gpu_lib.w4a16_gemm_launch_info(M, N, K, 128, 0, True)
+    if fused["path"] == gpu_lib.W4A16_PATH_SMALL_M:
+        assert fused["ctas"] == -(-N // 128) * fused["split"] * 2
+    else:
+        assert fused["ctas"] % -(-N // 64) == 0
