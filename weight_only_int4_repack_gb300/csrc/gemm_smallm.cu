@@ -187,11 +187,17 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
     // Metadata of the first chunk, first batch of 8 groups per row: the loads are
     // issued before the barrier that releases the weight stream, so they are
     // ahead of it in the memory system (they are latency-critical, it is not).
+    // In the common format (fp16 scales, G % 8 == 0) the raw words are kept and
+    // converted after the barrier, so that no thread waits for them there and the
+    // copies start at once.
     constexpr int RPT = (kTileRows + NC - 1) / NC;  // metadata rows per consumer thread
     const int zpstride = (p.G + 1) / 2;
     constexpr int PREB = RPT == 1 ? 2 : 1;  // prefetched batches of 8 groups
+    const bool raw_meta = !p.scale_f32 && (p.G & 7) == 0;
     float pre_s[RPT][PREB][8];
     uint32_t pre_z[RPT][PREB][8];
+    uint4 pre_x[RPT][PREB];       // raw fp16 scales of a batch (common format)
+    uint32_t pre_zw[RPT][PREB];   // raw zero-point bytes of a batch (common format)
     // One batch = the 8 groups gbase .. gbase+7 of one row (gbase a multiple of 8);
     // groups outside [lo, hi) are not needed. fp16 scales in rows that start 16-byte
     // aligned (G % 8 == 0) come from one 16-byte load, their zero points from one
@@ -233,6 +239,17 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
             }
         }
     };
+    // Raw words of one batch (common format); a window that holds none of the
+    // needed groups is not loaded (it may lie past the end of the row).
+    auto load_raw_batch = [&](int row, int gbase, int lo, int hi, uint4 &x, uint32_t &zw) {
+        x = make_uint4(0u, 0u, 0u, 0u);
+        zw = 0x88888888u;
+        if (row >= R || gbase >= hi || gbase + 8 <= lo) return;
+        const int n = n0 + row;
+        x = __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned short *>(set_scales) +
+                                                  (size_t)n * p.G + gbase));
+        if (set_zp) zw = __ldg(reinterpret_cast<const unsigned int *>(set_zp + (size_t)n * zpstride + gbase / 2));
+    };
     const int grp_first0 = (b_begin * kKBlock) / GROUP;
     const int ng_first0 = ((min(b_begin + kc, b_end) - b_begin) * kKBlock) / GROUP;
     if (warp < CW) {
@@ -241,9 +258,13 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
             const int rs = tid + NC * r;
             if (rs < kTileRows) {
 #pragma unroll
-                for (int bt = 0; bt < PREB; ++bt)
-                    load_meta_batch(rs, (grp_first0 & ~7) + 8 * bt, grp_first0, grp_first0 + ng_first0, pre_s[r][bt],
-                                    pre_z[r][bt]);
+                for (int bt = 0; bt < PREB; ++bt) {
+                    const int gbase = (grp_first0 & ~7) + 8 * bt;
+                    if (raw_meta)
+                        load_raw_batch(rs, gbase, grp_first0, grp_first0 + ng_first0, pre_x[r][bt], pre_zw[r][bt]);
+                    else
+                        load_meta_batch(rs, gbase, grp_first0, grp_first0 + ng_first0, pre_s[r][bt], pre_z[r][bt]);
+                }
             }
         }
     }
@@ -350,7 +371,16 @@ __global__ void __launch_bounds__(Shape<MT, SWIGLU>::THREADS, Shape<MT, SWIGLU>:
                     const int bt = (gb - gbase0) >> 3;
                     float sv[8];
                     uint32_t zb[8];
-                    if (c0 == b_begin && bt < PREB) {
+                    if (c0 == b_begin && bt < PREB && raw_meta) {
+                        const uint4 x = bt == 0 ? pre_x[r][0] : pre_x[r][PREB - 1];
+                        const uint32_t zw = bt == 0 ? pre_zw[r][0] : pre_zw[r][PREB - 1];
+                        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            sv[u] = __half2float(__ushort_as_half((unsigned short)(xs[u >> 1] >> (16 * (u & 1)))));
+                            zb[u] = (zw >> (8 * (u >> 1))) & 0xFFu;
+                        }
+                    } else if (c0 == b_begin && bt < PREB) {
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
                             sv[u] = bt == 0 ? pre_s[r][0][u] : pre_s[r][PREB - 1][u];
