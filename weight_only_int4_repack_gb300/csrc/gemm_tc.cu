@@ -8,25 +8,30 @@
 //     operand (N = T tokens, 16..256) staged by TMA with the 128-byte swizzle;
 //     D = W . A^T accumulates in fp32 in tensor memory;
 //   * a producer warp issues, per 64-k block, one TMA box of activations and one
-//     cp.async.bulk copy of the weight chunk (4 KB contiguous in the repacked
-//     layout) into a ring of shared-memory stages;
-//   * eight dequant warps, two per tensor-memory lane quarter (one thread per
-//     weight row, i.e. per lane; each of the two covers half the k16 steps), read
-//     their row's nibbles from the chunk (conflict-free thanks to the layout's
-//     lane-slot rotation), form w = (q - zp) * s in fp16 (nibbles OR-ed into the
-//     mantissa of 1024, one exact subtraction of 1024 + zp, one multiply by the
-//     scale) and store 16 packed columns each with tcgen05.st;
-//   * the shared-memory ring (TMA latency) is deeper than the tensor-memory ring
-//     of A stages (capacity-limited); each has its own "empty" barrier;
+//     3-D TMA box of the weight chunk (eight 512-byte sub-tile pieces of the
+//     repacked layout, 4 KB) into a ring of shared-memory stages;
+//   * three groups of four dequant warps (one warp per tensor-memory lane
+//     quarter, one thread per weight row) take every third k-block: a thread
+//     reads its row's nibbles from the chunk (conflict-free thanks to the
+//     layout's lane-slot rotation), forms w = (q - zp) * s in fp16 (nibbles
+//     OR-ed into the mantissa of 1024, one exact subtraction of 1024 + zp, one
+//     multiply by the scale) and stores the block's 32 packed columns with one
+//     tcgen05.st;
+//   * the shared-memory ring of copies and the tensor-memory ring of A stages
+//     advance together, one "empty" barrier per stage freeing both;
 //   * one thread issues the four K=16 MMAs per block and commits them to the
-//     "empty" barriers; after the last block a commit releases the epilogue (the
-//     same eight warps), which reads the accumulator with tcgen05.ld and stores
-//     fp16;
+//     stage's "empty" barrier; it issues every MMA of the CTA, so its
+//     instructions per block set the block period (each barrier wait, MMA and
+//     commit of that thread costs tens of nanoseconds): it waits only on the A
+//     stage, which the dequant warps fill after they have seen the copies land;
+//     after the last block a commit releases the epilogue (the dequant warps),
+//     which reads the accumulator with tcgen05.ld and stores fp16;
 //   * fused SwiGLU keeps the plain GEMM's 256-token tile: a CTA owns 64 output
-//     columns, and its 128 MMA rows are those 64 gate rows followed by the same
-//     64 up rows (two 2 KB halves of the repacked chunks), so one accumulator
-//     holds both and every dequantised weight still serves 256 tokens. The
-//     epilogue pairs row r with row r + 64 through shared memory and stores
+//     columns, and its 128 MMA rows are those 64 gate rows and the same 64 up
+//     rows (two 2 KB halves of the repacked chunks), interleaved by 16 so that
+//     each lane quarter holds the gate and the up rows of 16 columns; one
+//     accumulator holds both, every dequantised weight still serves 256 tokens,
+//     and the epilogue pairs lane l with lane l ^ 16 by a shuffle and stores
 //     silu(gate) * up.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // W4A16_ERR_TIMEOUT, drains what it issued, frees its tensor memory and returns.
@@ -57,6 +62,7 @@ struct TcShape {
     static constexpr int STAGES = 6;    // shared-memory ring (TMA in flight)
     static constexpr int ASTAGES = 6;   // tensor-memory A stages: T + ASTAGES*32 <= 512
     static_assert(STAGES % kDqParts == 0 && ASTAGES % kDqParts == 0, "ring depths: multiples of the dequant groups");
+    static_assert(STAGES == ASTAGES, "one barrier frees a shared-memory stage and its tensor-memory A stage");
 };
 
 // ------------------------------------------------------------------ tcgen05
@@ -177,7 +183,7 @@ __host__ __device__ inline TcSmem tc_smem(int T, int stages, int astages, int ns
     p.b_stage = (size_t)T * 128;  // T token rows x 64 fp16
     p.w_off = p.b_stage * stages;
     p.bar_off = p.w_off + (size_t)stages * ns * kChunk;
-    p.total = p.bar_off + (size_t)(2 * stages + 2 * astages + 2) * 8 + 16;
+    p.total = p.bar_off + (size_t)(2 * stages + astages + 2) * 8 + 16;
     return p;
 }
 
@@ -223,10 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const TcSmem L = tc_smem(T, STAGES, ASTAGES, NS);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);  // TMA + bulk copy landed
-    uint64_t *empty = full + STAGES;                                  // MMAs done with the smem stage
-    uint64_t *afull = empty + STAGES;                                 // A stage written to tensor memory
-    uint64_t *aempty = afull + ASTAGES;                               // MMAs done with the A stage
-    uint64_t *accfull = aempty + ASTAGES;
+    uint64_t *empty = full + STAGES;    // MMAs done with the stage (shared memory and A columns)
+    uint64_t *afull = empty + STAGES;   // A stage written to tensor memory
+    uint64_t *accfull = afull + ASTAGES;
     uint64_t *drain = accfull + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -243,10 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
-        for (int s = 0; s < ASTAGES; ++s) {
-            ptx::mbar_init(&afull[s], kDqThreads / kDqParts);  // one warp group per block
-            ptx::mbar_init(&aempty[s], 1);
-        }
+        for (int s = 0; s < ASTAGES; ++s) ptx::mbar_init(&afull[s], kDqThreads / kDqParts);  // one warp group per block
         ptx::mbar_init(accfull, 1);
         ptx::mbar_init(drain, 1);
         *abort_flag = 0;
@@ -268,19 +270,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::prefetch_tmap(&tmap_a);
             ptx::prefetch_tmap(&tmap_w0);
             if (SWIGLU) ptx::prefetch_tmap(&tmap_w1);
-            int kb = 0;
+            const uint32_t tx_bytes = (uint32_t)L.b_stage + (uint32_t)kChunk;
+            int kb = 0, s = 0;
+            uint32_t ph = 0;
             for (; kb < nkb; ++kb) {
-                const int s = kb % STAGES;
-                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
                 if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err, p.wait_ns)) break;
                 // One box of COLS/16 sub-tiles x one k-block per weight set (sub-tiles
                 // past N read as zero), full size in bytes whatever the ragged edge.
-                ptx::mbar_arrive_expect_tx(&full[s], (uint32_t)L.b_stage + (uint32_t)kChunk);
+                ptx::mbar_arrive_expect_tx(&full[s], tx_bytes);
                 ptx::tma_load_2d(smem + (size_t)s * L.b_stage, &tmap_a, kb * kKBlock, m0, &full[s]);
                 unsigned char *wdst = smem + L.w_off + (size_t)s * kChunk;
                 ptx::tma_load_3d_hint(wdst, &tmap_w0, 0, kb, sub0, &full[s], stream_policy);
                 if (SWIGLU)  // up rows in the second half of the slot
                     ptx::tma_load_3d_hint(wdst + kChunk / 2, &tmap_w1, 0, kb, sub0, &full[s], stream_policy);
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             if (*abort_flag) {  // let issued copies land before the CTA can exit
                 volatile int no_abort = 0;
@@ -293,27 +299,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // This one thread issues every MMA of the CTA and shares its scheduler with
+        // three busy dequant warps, so its instructions per block set the block
+        // period: descriptors and tensor-memory addresses advance by constant steps
+        // and the stage counters run without divisions.
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(T);
-            int kb = 0;
+            // Start-address field of the descriptor in 16-byte units: +b_stage/16 per
+            // stage, +2 per k16 step (32 bytes); shared addresses stay below 2^18, so
+            // the 14-bit field never carries.
+            const uint64_t bdesc0 = smem_desc_sw128(ptx::smem_u32(smem));
+            const uint32_t bstage = (uint32_t)(L.b_stage >> 4);
+            const uint32_t d_acc = tmem + acc_col, a_base0 = tmem + a_col0;
+            int kb = 0, s = 0;  // stage of both rings
+            uint32_t ph = 0;
             for (; kb < nkb; ++kb) {
-                const int s = kb % STAGES, sa = kb % ASTAGES;
-                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u, pa = (uint32_t)(kb / ASTAGES) & 1u;
-                if (!ptx::mbar_wait(&full[s], ph, abort_flag, p.err, p.wait_ns)) break;
-                if (!ptx::mbar_wait(&afull[sa], pa, abort_flag, p.err, p.wait_ns)) break;
+                // The dequant group arrives on afull only after it has itself waited for
+                // this stage's copies (weights and activations alike), so a completed
+                // afull phase implies a completed full phase: no second wait here.
+                if (!ptx::mbar_wait(&afull[s], ph, abort_flag, p.err, p.wait_ns)) break;
                 tc_fence_after();
-                const uint32_t b_base = ptx::smem_u32(smem + (size_t)s * L.b_stage);
+                const uint64_t bdesc = bdesc0 + (uint64_t)((uint32_t)s * bstage);
+                const uint32_t a_base = a_base0 + (uint32_t)(s * NS * 32);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint64_t bdesc = smem_desc_sw128(b_base + 32u * j);  // k16 step j: +32 bytes
 #pragma unroll
                     for (int w = 0; w < NS; ++w)
-                        tc_mma(tmem + acc_col + (uint32_t)(w * T),
-                               tmem + a_col0 + (uint32_t)((sa * NS + w) * 32 + 8 * j), bdesc, idesc,
+                        tc_mma(d_acc + (uint32_t)(w * T), a_base + (uint32_t)(w * 32 + 8 * j), bdesc + 2u * j, idesc,
                                (kb > 0 || j > 0) ? 1u : 0u);
                 }
-                tc_commit(&empty[s]);    // frees the shared-memory stage
-                tc_commit(&aempty[sa]);  // frees the tensor-memory A stage
+                tc_commit(&empty[s]);  // frees the shared-memory and tensor-memory stages
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             if (kb == nkb) {
                 tc_commit(accfull);
@@ -351,10 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bool aborted = false;
         for (int kb = hf; kb < nkb; kb += kDqParts) {
-            const int s = kb % STAGES, sa = kb % ASTAGES;
-            const uint32_t ph = (uint32_t)(kb / STAGES) & 1u, pa = (uint32_t)(kb / ASTAGES) & 1u;
+            const int s = kb % STAGES;  // stage of both rings
+            const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
             if (!aborted && !ptx::mbar_wait(&full[s], ph, abort_flag, p.err, p.wait_ns)) aborted = true;
-            if (!aborted && !ptx::mbar_wait(&aempty[sa], pa ^ 1u, abort_flag, p.err, p.wait_ns)) aborted = true;
+            if (!aborted && !ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err, p.wait_ns)) aborted = true;
             if (aborted) break;
             // The group's next block's metadata, loaded early (it is used one block later).
             const int kbn = kb + kDqParts;
@@ -398,12 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 8 * kSPW; ++c) col[c] = 0u;
                 }
-                const uint32_t ta = tmem + lane_base + a_col0 + (uint32_t)((sa * NS + w) * 32);
+                const uint32_t ta = tmem + lane_base + a_col0 + (uint32_t)((s * NS + w) * 32);
                 tmem_st_cols(ta, col);
             }
             tmem_wait_st();
             tc_fence_before();
-            ptx::mbar_arrive(&afull[sa]);
+            ptx::mbar_arrive(&afull[s]);
             if (kbn < nkb) {
 #pragma unroll
                 for (int w = 0; w < NS; ++w)
