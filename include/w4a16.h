@@ -154,6 +154,28 @@ w4a16_status w4a16_gemm(const uint16_t *A, const uint8_t *q_rep, const void *sca
                         void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * w4a16_gemm for a caller whose activations arrive and whose outputs leave in
+ * host memory (the same operation, defined at the top of this file): enqueues on
+ * `stream` the copy of A_host into A_dev, the GEMM into Y_dev and the copy of
+ * Y_dev into Y_host, one cudaMemcpyAsync per copy, and returns without
+ * synchronising; Y_host holds the result once the stream has passed the call.
+ *   A_host   host fp16 [M][K], page-locked (cudaHostAlloc, cudaHostRegister or
+ *            torch pin_memory); not checked: with pageable memory the CUDA
+ *            runtime performs the copies synchronously
+ *   A_dev    device fp16 [M][K], 16-byte aligned, overwritten with A_host
+ *   Y_dev    device fp16 [M][N], 16-byte aligned, overwritten with Y
+ *   Y_host   host fp16 [M][N], page-locked as A_host, overwritten with Y
+ *   q_rep, scales, sdt, zp, group, split_k as in w4a16_gemm (no workspace)
+ * Every argument is validated before anything is enqueued, with the errors of
+ * w4a16_gemm; a CUDA failure after the first copy was enqueued returns
+ * W4A16_ERR_CUDA and may leave that copy enqueued.
+ */
+w4a16_status w4a16_gemm_host_io(const uint16_t *A_host, uint16_t *A_dev, const uint8_t *q_rep,
+                                const void *scales, w4a16_scale_dtype sdt, const uint8_t *zp,
+                                uint16_t *Y_dev, uint16_t *Y_host, int M, int N, int K, int group,
+                                int split_k, void *stream);
+
+/*
  * Scratch bytes for w4a16_gemm_swiglu: 0 when fused; 4*M*N (+alignment) when
  * unfused (the fp16 gate and up projections are materialised).
  */

@@ -89,6 +89,21 @@ def test_gemm_validation(w4, kw, status):
     assert _gemm(w4, **kw) == status
 
 
+def _host_io(w4, Ah=0x30000, A=A16, q=A16, s=A16, sdt=0, zp=None, Y=A16, Yh=0x40000, M=8, N=256, K=512,
+             group=64, split=0):
+    return w4.lib.w4a16_gemm_host_io(Ah, A, q, s, sdt, zp, Y, Yh, M, N, K, group, split, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Ah=None), 1), (dict(Yh=None), 1), (dict(A=None), 1), (dict(Y=None), 1),
+    (dict(A=BAD), 1), (dict(Y=BAD), 1), (dict(q=None), 1), (dict(sdt=7), 1),
+    (dict(M=0), 1), (dict(N=200), 2), (dict(group=48), 2), (dict(split=9), 1),
+])
+def test_host_io_validation(w4, kw, status):
+    # Every check runs before the first copy is enqueued (no device is touched).
+    assert _host_io(w4, **kw) == status
+
+
 def test_swiglu_workspace_validation(w4):
     lib = w4.lib
     args = [A16, A16, A16, None, A16, A16, None, 0, A16, 8, 256, 512, 64]

@@ -44,7 +44,7 @@ EXPORTS = (
     "w4a16_swiglu_workspace_bytes", "w4a16_gemm_swiglu", "w4a16_set_tuning", "w4a16_set_launch_overlap",
     "w4a16_device_error", "w4a16_swiglu_static_scratch_bytes", "w4a16_gemm_swiglu_unfused_static",
     "w4a16_set_wait_limit_ns", "w4a16_rmsnorm_workspace_bytes", "w4a16_gemm_rmsnorm",
-    "w4a16_gemm_swiglu_rmsnorm", "w4a16_gemm_launch_info",
+    "w4a16_gemm_swiglu_rmsnorm", "w4a16_gemm_launch_info", "w4a16_gemm_host_io",
 )
 
 _vp, _ci, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -68,6 +68,7 @@ _sig = {
     "w4a16_gemm_plan": (_ci, [_ci, _ci, _ci, _ci, _ci, ctypes.POINTER(_ci), ctypes.POINTER(_ci)]),
     "w4a16_gemm_launch_info": (_ci, [_ci, _ci, _ci, _ci, _ci, _ci, ctypes.POINTER(LaunchInfo)]),
     "w4a16_gemm": (_ci, [_vp, _vp, _vp, _ci, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _vp, _sz, _vp]),
+    "w4a16_gemm_host_io": (_ci, [_vp, _vp, _vp, _vp, _ci, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _vp]),
     "w4a16_swiglu_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci]),
     "w4a16_gemm_swiglu": (_ci, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _vp,
                                 _ci, _ci, _ci, _ci, _ci, _vp, _sz, _vp]),
@@ -183,6 +184,19 @@ def w4a16_gemm(A, q_rep, scales, zp, group: int, out=None, split_k: int = 0, wor
                           _ptr(out), M, N, K, group, split_k, _ptr(workspace), ws_bytes,
                           _stream(stream)), "w4a16_gemm")
     return out
+
+
+def w4a16_gemm_host_io(A_host, A_dev, q_rep, scales, zp, group: int, Y_dev, Y_host, split_k: int = 0,
+                       stream=None):
+    """Copy A_host (pinned CPU fp16 [M, K]) into A_dev, run the GEMM into Y_dev and
+    copy it into Y_host (pinned CPU fp16 [M, N]), all enqueued on the stream; no
+    synchronisation (Y_host is valid once the stream has passed the call)."""
+    M, K = A_host.shape
+    N = scales.shape[0]
+    _check(lib.w4a16_gemm_host_io(_ptr(A_host), _ptr(A_dev), _ptr(q_rep), _ptr(scales), _scale_dtype(scales),
+                                  _ptr(zp), _ptr(Y_dev), _ptr(Y_host), M, N, K, group, split_k,
+                                  _stream(stream)), "w4a16_gemm_host_io")
+    return Y_host
 
 
 def w4a16_swiglu_workspace_bytes(M, N, K, group, fused) -> int:

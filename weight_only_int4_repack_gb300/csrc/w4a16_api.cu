@@ -394,6 +394,25 @@ w4a16_status w4a16_gemm(const uint16_t *A, const uint8_t *q_rep, const void *sca
     return gemm_impl(A, &w, 1, sdt, Y, M, N, K, group, split_k, (cudaStream_t)stream);
 }
 
+w4a16_status w4a16_gemm_host_io(const uint16_t *A_host, uint16_t *A_dev, const uint8_t *q_rep,
+                                const void *scales, w4a16_scale_dtype sdt, const uint8_t *zp,
+                                uint16_t *Y_dev, uint16_t *Y_host, int M, int N, int K, int group,
+                                int split_k, void *stream) {
+    w4a16_status st = check_shape(M, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (!A_host || !A_dev || !Y_dev || !Y_host) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(A_dev, 16) || !aligned(Y_dev, 16)) return W4A16_ERR_INVALID_ARG;
+    if ((st = check_weights(q_rep, scales, sdt)) != W4A16_OK) return st;
+    Plan plan;  // the plan's checks (split_k, shape) before the first copy is enqueued
+    if ((st = make_plan(M, N, K, group, split_k, false, sdt == W4A16_SCALE_F32, &plan)) != W4A16_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    st = from_cuda(cudaMemcpyAsync(A_dev, A_host, (size_t)M * K * 2, cudaMemcpyHostToDevice, s));
+    if (st != W4A16_OK) return st;
+    const WeightSet w{q_rep, scales, zp};
+    if ((st = gemm_impl(A_dev, &w, 1, sdt, Y_dev, M, N, K, group, split_k, s)) != W4A16_OK) return st;
+    return from_cuda(cudaMemcpyAsync(Y_host, Y_dev, (size_t)M * N * 2, cudaMemcpyDeviceToHost, s));
+}
+
 size_t w4a16_swiglu_workspace_bytes(int M, int N, int K, int group, int fused) {
     (void)K; (void)group;
     if (fused || M <= 0 || N <= 0) return 0;
