@@ -20,10 +20,10 @@
 //   * the shared-memory ring of copies and the tensor-memory ring of A stages
 //     advance together, one "empty" barrier per stage freeing both;
 //   * one thread issues the four K=16 MMAs per block and commits them to the
-//     stage's "empty" barrier; it issues every MMA of the CTA, so its
-//     instructions per block set the block period (each barrier wait, MMA and
-//     commit of that thread costs tens of nanoseconds): it waits only on the A
-//     stage, which the dequant warps fill after they have seen the copies land;
+//     stage's "empty" barrier; it issues every MMA of the CTA and each of its
+//     barrier waits, MMAs and commits costs tens of nanoseconds, so it waits
+//     only on the A stage, which the dequant warps fill after they have seen the
+//     copies land, and commits once per block;
 //     after the last block a commit releases the epilogue (the dequant warps),
 //     which reads the accumulator with tcgen05.ld and stores fp16;
 //   * fused SwiGLU keeps the plain GEMM's 256-token tile: a CTA owns 64 output
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // This one thread issues every MMA of the CTA and shares its scheduler with
-        // three busy dequant warps, so its instructions per block set the block
+        // three busy dequant warps, so its instructions per block weigh on the block
         // period: descriptors and tensor-memory addresses advance by constant steps
         // and the stage counters run without divisions.
         if (lane == 0) {
